@@ -1,0 +1,524 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode step (KV GB/s, % of measured HBM peak, KV tokens/s).
+
+One step = the whole hot path over one batch: copy-on-write block copies (when the
+workload has them), slot mapping + cache write of every new token, then decode
+attention (plan, split-KV attention, merge) and chunked-prefill attention (when the
+workload has a prefill batch).  Default workload: the Llama-3.1-8B-shaped GQA decode
+layer (256 sequences, 32 query / 8 KV heads, head dim 128, bf16, block size 16,
+lognormal context lengths).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  `value` is KV bytes read per step / device time per step
+(GB/s) with every input resident in HBM; `e2e` repeats the measurement through the same
+C-ABI calls with the step's inputs copied from pinned host memory and the output copied
+back inside the timed region.  The reference arm (`--impl reference`) times the CPU
+oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; KV tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_53_gb300", "csrc", "pa_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+# ------------------------------------------------------------------ accounting
+def kv_bytes(step: W.Step) -> int:
+    """K and V bytes one decode over the step reads: each context token's K and V row for
+    every KV head, once."""
+    sh = step.shape
+    return int(step.decode.context_lens.astype(np.int64).sum()) * 2 * sh.num_kv_heads * \
+        sh.head_dim * sh.elem_bytes
+
+
+def decode_algorithmic_bytes(step: W.Step, out_bytes: int) -> int:
+    """Algorithmic HBM bytes of one decode call: KV rows, q, the output, the block-table
+    entries walked and the context lengths."""
+    sh, b = step.shape, step.decode
+    blocks = int(((b.context_lens.astype(np.int64) + sh.block_size - 1) // sh.block_size).sum())
+    q = b.num_seqs * sh.num_q_heads * sh.head_dim * sh.elem_bytes
+    o = b.num_seqs * sh.num_q_heads * sh.head_dim * out_bytes
+    return kv_bytes(step) + q + o + 4 * blocks + 4 * b.num_seqs
+
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.dirname(DECODE_SRC))):
+        with open(os.path.join(os.path.dirname(DECODE_SRC), f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """ncu DRAM bytes per decode-kernel launch for this workload, if they were taken on
+    the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        e = rec.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_53_gb300 as pa
+    import paged_kv_cache_53_gb300.build as pabuild
+
+    pabuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    step = W.NAMED[args.workload]()
+    if world > 1:  # each rank serves its own batch: independent units, no exchange
+        step = W.replace(step, seed=step.seed + 1000 * rank)
+    sh = step.shape
+    vals = W.make_values(step, dev)
+    kc, vc = vals["k_cache"], vals["v_cache"]
+    tdt = kc.dtype
+    stream = torch.cuda.current_stream(dev)
+
+    meta = {}
+    for kind in ("decode", "prefill"):
+        b = getattr(step, kind)
+        if b is None:
+            continue
+        meta[kind] = {
+            "bt": torch.from_numpy(b.block_tables).to(dev),
+            "ctx": torch.from_numpy(b.context_lens).to(dev),
+            "cu": torch.from_numpy(b.cu_q_lens).to(dev),
+            "slots": torch.empty(b.num_new_tokens, dtype=torch.int64, device=dev),
+        }
+    pairs = torch.from_numpy(step.cow_pairs).to(dev) if step.cow_pairs is not None else None
+    d = step.decode
+    out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
+    ws_dec = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads, sh.num_kv_heads,
+                                                   sh.head_dim, d.max_ctx, sh.block_size),
+                         dtype=torch.uint8, device=dev)
+    p = step.prefill
+    if p is not None:
+        out_pre = torch.empty((p.num_new_tokens, sh.num_q_heads, sh.head_dim), dtype=tdt,
+                              device=dev)
+        nbytes = pa.prefill_workspace_bytes(p.num_seqs, p.num_new_tokens, p.max_q,
+                                            sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
+                                            p.max_ctx, sh.block_size)
+        ws_pre = torch.empty(max(16, nbytes), dtype=torch.uint8, device=dev)
+
+    launches_per_step = 0
+
+    def one_step(q_dec, ev=None):
+        nonlocal launches_per_step
+        n = 0
+        if pairs is not None:
+            pa.copy_blocks([kc], [vc], pairs)
+            n += 1
+        for kind, m in meta.items():
+            pa.slot_mapping(m["slots"], m["bt"], m["cu"], m["ctx"], sh.block_size, step.num_blocks)
+            pa.reshape_and_cache(vals[f"k_new_{kind}"], vals[f"v_new_{kind}"], kc, vc, m["slots"])
+            n += 2
+        if ev is not None:
+            ev[0].record(stream)
+        pa.decode(out_dec, q_dec, kc, vc, meta["decode"]["bt"], meta["decode"]["ctx"], d.max_ctx,
+                  step.scale, ws_dec)
+        if ev is not None:
+            ev[1].record(stream)
+        n += 3  # plan, attend, merge
+        if p is not None:
+            pa.prefill_chunk(out_pre, vals["q_prefill"], kc, vc, meta["prefill"]["bt"],
+                             meta["prefill"]["cu"], meta["prefill"]["ctx"], p.max_q, p.max_ctx,
+                             step.scale, ws_pre)
+            n += 1
+        launches_per_step = n
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # warm-up
+    for _ in range(args.warmup):
+        one_step(vals["q_decode"])
+    barrier()
+    if pa.get_status() != 0:
+        raise RuntimeError("library status word set during warm-up")
+
+    # timed region: inputs resident in HBM
+    k = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(k)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        t0.record(stream)
+        for i in range(k):
+            one_step(vals["q_decode"], evs[i])
+        t1.record(stream)
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    if pa.get_status() != 0:
+        raise RuntimeError("library status word set during the timed region")
+
+    # end to end: the step's inputs from pinned host memory, the output back to the host
+    h_q = vals["q_decode"].cpu().pin_memory()
+    h_new = {key: vals[key].cpu().pin_memory() for key in vals if key.startswith(("k_new", "v_new"))}
+    if p is not None:
+        h_qp = vals["q_prefill"].cpu().pin_memory()
+    h_meta = {kind: {n: m[n].cpu().pin_memory() for n in ("bt", "ctx", "cu")}
+              for kind, m in meta.items()}
+    h_out = torch.empty(out_dec.shape, dtype=tdt).pin_memory()
+    d_q = torch.empty_like(vals["q_decode"])
+    h2d = h_q.numel() * h_q.element_size() + sum(t.numel() * t.element_size() for t in h_new.values())
+    h2d += sum(t.numel() * t.element_size() for m in h_meta.values() for t in m.values())
+    if p is not None:
+        h2d += h_qp.numel() * h_qp.element_size()
+    d2h = h_out.numel() * h_out.element_size()
+    ke = max(1, min(k, args.e2e_steps))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        d_q.copy_(h_q, non_blocking=True)
+        for key, t in h_new.items():
+            vals[key].copy_(t, non_blocking=True)
+        for kind, m in h_meta.items():
+            for n, t in m.items():
+                meta[kind][n].copy_(t, non_blocking=True)
+        if p is not None:
+            vals["q_prefill"].copy_(h_qp, non_blocking=True)
+        one_step(d_q)
+        h_out.copy_(out_dec, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / ke
+
+    step_ms = total_ms / k
+    times = np.array([step_ms, dec_ms, e2e_ms], dtype=np.float64)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor(times, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.cpu().numpy()
+    step_ms, dec_ms, e2e_ms = [float(x) for x in times]
+
+    kvb = kv_bytes(step)
+    kv_tokens = int(d.context_lens.astype(np.int64).sum())
+    value = world * kvb / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    alg = decode_algorithmic_bytes(step, out_dec.element_size())
+    achieved = alg / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": k,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": sh.dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": step.name,
+            "num_seqs": d.num_seqs, "num_q_heads": sh.num_q_heads,
+            "num_kv_heads": sh.num_kv_heads, "head_dim": sh.head_dim,
+            "block_size": sh.block_size, "kv_tokens_per_step": kv_tokens,
+            "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
+            "prefill_tokens": p.num_new_tokens if p is not None else 0,
+            "cow_copies": int(step.cow_pairs.shape[0]) if step.cow_pairs is not None else 0,
+            "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV read per step vs 0.13 GB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),
+        "hbm_frac_of_measured": round(value / peak, 4),
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 5), "steps": ke},
+        "gpu_launches": launches_per_step * k,
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (plan + attend + merge)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": alg,
+                     "ms_per_launch": round(dec_ms, 5)},
+    }
+    return res, step
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def _oracle_worker(payload):
+    """Runs the oracle decode over one chunk of sequences; returns (seconds, kv tokens)."""
+    import oracle
+    (q, kc, vc, tables, ctx, scale, dtype) = payload
+    t = time.perf_counter()
+    oracle.decode_attention(q, kc, vc, tables, ctx, scale, dtype)
+    return time.perf_counter() - t, int(ctx.astype(np.int64).sum())
+
+
+def _oracle_payload(step: W.Step, seqs, gen):
+    """The listed sequences of the workload with a pool of just their blocks (random
+    values, same shapes and lengths), tables renumbered into that pool."""
+    import torch  # noqa: F401
+    sh, d = step.shape, step.decode
+    ctx = d.context_lens[seqs].astype(np.int32)
+    nblk = (ctx.astype(np.int64) + sh.block_size - 1) // sh.block_size
+    total = int(nblk.sum())
+    kc = W.to_numpy(W.randn((total, sh.num_kv_heads, sh.block_size, sh.head_dim), sh.dtype,
+                            "cpu", gen))
+    vc = W.to_numpy(W.randn((total, sh.num_kv_heads, sh.block_size, sh.head_dim), sh.dtype,
+                            "cpu", gen))
+    q = W.to_numpy(W.randn((len(seqs), sh.num_q_heads, sh.head_dim), sh.dtype, "cpu", gen))
+    tables = np.full((len(seqs), int(nblk.max())), -1, dtype=np.int32)
+    start = 0
+    for i, n in enumerate(nblk):
+        tables[i, :n] = np.arange(start, start + n)
+        start += n
+    return (q, kc, vc, tables, ctx, step.scale, sh.dtype)
+
+
+def make_oracle_sample(step: W.Step, budget_s: float, cores: int):
+    """Chooses a sample of sequences worth about `budget_s` seconds of oracle work per
+    core (measured on one sequence first) and splits it into per-worker payloads."""
+    import torch
+    d = step.decode
+    gen = torch.Generator().manual_seed(step.seed)
+    order = np.random.default_rng(7).permutation(d.num_seqs)
+    probe = _oracle_payload(step, [int(order[0])], gen)
+    secs, toks = _oracle_worker(probe)
+    per_token = secs / max(1, toks)
+    want = budget_s * cores / max(per_token, 1e-9)
+    seqs, tok = [], 0
+    for s in order:
+        if seqs and tok >= want:
+            break
+        seqs.append(int(s))
+        tok += int(d.context_lens[s])
+    chunks = [c for c in (seqs[i::cores] for i in range(cores)) if c]
+    payloads = [_oracle_payload(step, c, gen) for c in chunks]
+    kvb = tok * 2 * step.shape.num_kv_heads * step.shape.head_dim * step.shape.elem_bytes
+    desc = (f"{len(seqs)} of {d.num_seqs} sequences ({tok} of {int(d.context_lens.sum())} "
+            f"KV tokens) of the same workload; float64 numpy oracle in {len(payloads)} "
+            f"spawned single-threaded workers")
+    return payloads, desc, kvb
+
+
+class OraclePool:
+    """A spawned pool of single-threaded workers (started with spawn, so it is safe
+    after CUDA is initialised)."""
+
+    def __init__(self, n):
+        keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                               "MKL_NUM_THREADS")}
+        for k in keep:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(n)
+            self.pool.map(_noop, range(n))
+        finally:
+            for k, v in keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def time(self, payloads):
+        t = time.perf_counter()
+        self.pool.map(_oracle_worker, payloads, chunksize=1)
+        return time.perf_counter() - t
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _noop(_):
+    import oracle  # noqa: F401
+    return 0
+
+
+def host_cores():
+    return min(len(os.sched_getaffinity(0)), 16)
+
+
+def cpu_baseline(step: W.Step, budget_s: float):
+    cores = host_cores()
+    payloads, desc, kvb = make_oracle_sample(step, budget_s, cores)
+    pool = OraclePool(len(payloads))
+    try:
+        wall = pool.time(payloads)
+    finally:
+        pool.close()
+    return {"value": round(kvb / wall / 1e9, 4), "unit": "GB/s", "cores": len(payloads),
+            "kind": "oracle", "sample": desc, "seconds": round(wall, 2)}
+
+
+def run_reference(args, world):
+    step = W.NAMED[args.workload]()
+    cores = host_cores()
+    per_step = min(2.0, max(0.02, args.ref_total_s / max(1, args.steps + args.warmup)))
+    payloads, desc, kvb = make_oracle_sample(step, per_step, cores)
+    pool = OraclePool(len(payloads))
+    try:
+        for _ in range(args.warmup):
+            pool.time(payloads)
+        walls = [pool.time(payloads) for _ in range(args.steps)]
+    finally:
+        pool.close()
+    wall = float(np.mean(walls))
+    gbs = kvb / wall / 1e9
+    full = kv_bytes(step)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(full / (gbs * 1e9) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": step.name, "parallelism": "host cores",
+                   "sample_seconds_per_step": round(wall, 3)},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": len(payloads),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.NAMED), default="llama8b_gqa_decode")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget-s", type=float, default=2.0,
+                    help="seconds per core of oracle work for the cpu_baseline sample")
+    ap.add_argument("--ref-total-s", type=float, default=120.0,
+                    help="wall seconds the reference arm's timed steps may take in total")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world)), flush=True)
+        return 0
+
+    # the oracle's worker pool is spawned, so it may start after the GPU is in use
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res, step = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(step, args.cpu_budget_s)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache attention library (libpagedattn.so, sm_103a).
+ *
+ * The KV cache of one layer is a pool of fixed-size physical blocks.  A per-sequence
+ * block table maps each logical block of a sequence to the physical block holding it,
+ * so blocks need not be contiguous, and attention reads K/V through that table
+ * ("PagedAttention and Continuous Batching Explained (2026)", section "PagedAttention:
+ * a block table for the KV cache"; "KV Cache in Serving Engines: PagedAttention,
+ * Continuous Batching, and Prefix Caching", section "Blocks and Block Tables").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout.  K and V caches are separate arrays [num_blocks, num_kv_heads, block_size,
+ *   head_dim], row-major: token `off` of physical block `blk` for KV head `h` starts at
+ *   element ((blk * num_kv_heads + h) * block_size + off) * head_dim.  Block tables are
+ *   int32 [num_seqs, max_blocks_per_seq] row-major; entries past a sequence's last
+ *   block are never read.  Query/output rows are [tokens, num_q_heads, head_dim].
+ * Grouped-query attention.  Query head i reads KV head i / (num_q_heads / num_kv_heads).
+ * Context length.  context_lens[b] counts every token of sequence b once this step's
+ *   new tokens are in the cache (a decode's appended token included).
+ * Memory.  Every pointer argument named *_cache, q, out, k_new, v_new, block_tables,
+ *   context_lens, cu_q_lens, slot_mapping, pairs and workspace is a DEVICE pointer
+ *   owned by the caller and must be 16-byte aligned.  The library allocates no device
+ *   memory and keeps no state between calls except a per-device status word.
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
+ *   enqueues work on it and returns without synchronising.
+ * Errors.  A call returns PA_OK or a PA_ERR_* code.  Arguments are validated on the
+ *   host before anything is enqueued; on an error nothing is launched and
+ *   pa_last_error_string() (thread-local) says why.  Data-dependent faults found by the
+ *   kernels (a block id outside the pool, a slot outside the pool, a context longer
+ *   than its table) never trap: the offending access is skipped or reads zeros, and a
+ *   bit is set in the device status word read by pa_get_status().
+ * Supported shapes.  head_dim in {64, 128}; block_size in {16, 32};
+ *   num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.  dtype PA_F32, PA_F16, PA_BF16 for
+ *   cache writes, copies and decode; PA_F16 and PA_BF16 for chunked prefill.
+ */
+#ifndef PAGED_KV_CACHE_PA_H_
+#define PAGED_KV_CACHE_PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* return codes */
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, inconsistent shapes */
+#define PA_ERR_UNSUPPORTED 2 /* a head_dim, block_size, group size or dtype not built */
+#define PA_ERR_WORKSPACE 3   /* workspace smaller than the *_workspace_bytes() figure */
+#define PA_ERR_CUDA 4        /* the CUDA runtime refused a launch or a query */
+
+/* bits of the device status word */
+#define PA_STATUS_BAD_BLOCK 0x1   /* a block id outside [0, num_blocks) was met */
+#define PA_STATUS_BAD_SLOT 0x2    /* a slot outside [0, num_blocks * block_size) */
+#define PA_STATUS_BAD_CONTEXT 0x4 /* context < 0, or longer than max_ctx / its table */
+#define PA_STATUS_TIMEOUT 0x8     /* a pipeline wait in a kernel gave up (never expected) */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+/* Why the last call on this thread failed ("" after a success). */
+const char* pa_last_error_string(void);
+
+/* Reads the current device's status word into *status and clears it.  Synchronises
+ * the device.  Returns PA_ERR_CUDA if the device cannot be reached. */
+int pa_get_status(int32_t* status);
+
+/*
+ * pa_slot_mapping -- physical slot of every new token of a step.
+ *
+ * Blocks are allocated one at a time as a sequence grows, and each new token goes to
+ * the slot its position maps to through the table ("PagedAttention: a block table for
+ * the KV cache", page cited above).  Sequence b appends the tokens cu_q_lens[b] ..
+ * cu_q_lens[b+1]-1 of the step (one for a decode, a chunk for a prefill); they are the
+ * last positions of its context, so token t sits at position
+ *     pos = context_lens[b] - (cu_q_lens[b+1] - cu_q_lens[b]) + (t - cu_q_lens[b])
+ * and gets slot = block_tables[b][pos / block_size] * block_size + pos % block_size.
+ *
+ *   slots         int64 [num_tokens], written
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]
+ *   cu_q_lens     int32 [num_seqs + 1], cu_q_lens[0] = 0, cu_q_lens[num_seqs] = num_tokens
+ *   context_lens  int32 [num_seqs]
+ * A token whose position falls outside its table or whose block id is outside the pool
+ * gets slot -1 and sets a status bit.  Bit-exact.
+ */
+int pa_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                    int num_tokens, int block_size, int num_blocks, void* stream);
+
+/*
+ * pa_reshape_and_cache -- writes the new tokens' K and V into their slots.
+ *
+ *   k_new, v_new      [num_tokens, num_kv_heads, head_dim] of `dtype`
+ *   k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim] of `dtype`
+ *   slot_mapping      int64 [num_tokens]; a negative slot marks padding and is skipped;
+ *                     a slot >= num_blocks * block_size is skipped and sets a status bit
+ * Slots must be distinct within a call.  A bit copy: bit-exact.
+ */
+int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         void* stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write of shared blocks.
+ *
+ * Sequences may share physical blocks; a shared block is copied only when one of them
+ * must append to it ("KV Cache in Serving Engines", section "Sharing Blocks";
+ * "PagedAttention and Continuous Batching Explained (2026)", "Sharing").  For every
+ * pair (src, dst) and every layer, block dst of the K and the V cache becomes a copy
+ * of block src.
+ *
+ *   k_caches, v_caches  HOST arrays of `num_layers` DEVICE pointers, each a cache as in
+ *                       pa_reshape_and_cache (num_layers <= 256)
+ *   pairs               int32 [num_pairs, 2] (src, dst), device
+ * Destinations must be distinct and must not appear as a source in the same call.  A
+ * pair with an id outside [0, num_blocks) is skipped and sets a status bit.  Bit-exact.
+ */
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                   const int32_t* pairs, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode_workspace_bytes -- bytes of device workspace pa_decode needs for these
+ * sizes (the split-KV partial results and the work list).  max_ctx bounds every
+ * context length of the call.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int max_ctx, int block_size);
+
+/*
+ * pa_decode -- paged decode attention: one query token per sequence.
+ *
+ * For sequence b and query head i, with kv head h = i / (num_q_heads / num_kv_heads):
+ *     out[b][i] = sum_j softmax_j(scale * q[b][i] . K_b[j][h]) * V_b[j][h]
+ * over the context positions j < context_lens[b], where K_b and V_b are reached through
+ * row b of the block table.  This is the same attention as over a contiguous cache
+ * ("PagedAttention and Continuous Batching Explained (2026)", FAQ "Is PagedAttention a
+ * different attention algorithm?").  Long contexts are split into partitions whose
+ * partial results are merged by log-sum-exp rescaling.
+ *
+ *   out           [num_seqs, num_q_heads, head_dim] of out_dtype (dtype or PA_F32)
+ *   q             [num_seqs, num_q_heads, head_dim] of dtype
+ *   k/v_cache     [num_blocks, num_kv_heads, block_size, head_dim] of dtype
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens  int32 [num_seqs]; every entry must be <= max_ctx and <=
+ *                 max_blocks_per_seq * block_size (longer ones are clamped and set a
+ *                 status bit); a sequence with context 0 gets a zero output
+ *   workspace     device scratch of at least pa_decode_workspace_bytes(...) bytes; its
+ *                 contents need no initialisation and are overwritten
+ * Accumulation is fp32.  Two calls that share a workspace must not overlap in time.
+ */
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
+              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+              pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_prefill_workspace_bytes -- bytes of device workspace pa_prefill_chunk needs.
+ */
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int max_ctx,
+                                  int block_size);
+
+/*
+ * pa_prefill_chunk -- causal attention of a chunk of prompt tokens over paged context.
+ *
+ * Chunked prefill splits a long prompt into pieces processed in separate steps next to
+ * decodes ("PagedAttention and Continuous Batching Explained (2026)", section "Chunked
+ * prefill").  Sequence b owns query rows cu_q_lens[b] .. cu_q_lens[b+1]-1; its context
+ * holds context_lens[b] tokens INCLUDING the chunk, whose K/V must already be in the
+ * cache (call pa_reshape_and_cache first).  Query i of the chunk sits at position
+ * context_lens[b] - chunk_len + i and attends to positions 0 .. that position:
+ *     out[t][i] = sum_{j <= pos(t)} softmax_j(scale * q[t][i] . K_b[j][h]) * V_b[j][h]
+ *
+ *   out           [num_tokens, num_q_heads, head_dim] of out_dtype (dtype or PA_F32)
+ *   q             [num_tokens, num_q_heads, head_dim] of dtype (PA_F16 or PA_BF16)
+ *   cu_q_lens     int32 [num_seqs + 1]; max_q >= every chunk length
+ *   context_lens  int32 [num_seqs]; chunk_len <= context_lens[b] <= max_ctx
+ *   workspace     device scratch of pa_prefill_workspace_bytes(...) bytes (may be 0)
+ * QK^T and PV run on the tensor cores with fp32 accumulation.
+ */
+int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                     int num_tokens, int max_q, int max_ctx, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_CACHE_PA_H_ */

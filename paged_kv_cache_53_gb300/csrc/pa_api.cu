@@ -1,0 +1,382 @@
+// C-ABI entry points: host-side validation, error reporting, the device status word,
+// TMA descriptor encoding, and dispatch to the kernels' launchers.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+thread_local char g_error[512] = "";
+
+constexpr int kMaxDevices = 64;
+__device__ int32_t g_status_word;  // one per device that loads the library
+
+int32_t* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::mutex g_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+CUtensorMapDataType tma_dtype(pa_dtype dt) {
+  switch (dt) {
+    case PA_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case PA_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  }
+}
+
+// Checks shared by every attention / cache call.
+int check_cache_geometry(const char* fn, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int dtype) {
+  if (!valid_dtype(dtype)) return fail(PA_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
+  if (num_kv_heads <= 0 || num_blocks <= 0 || head_dim <= 0 || block_size <= 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: sizes must be positive (kv_heads=%d blocks=%d)", fn,
+                num_kv_heads, num_blocks);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not built (64, 128)", fn, head_dim);
+  if (block_size != 16 && block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "%s: block_size %d not built (16, 32)", fn, block_size);
+  const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+  if (rows >= (1ll << 31))
+    return fail(PA_ERR_INVALID_ARG, "%s: num_blocks * num_kv_heads * block_size = %lld >= 2^31",
+                fn, rows);
+  return PA_OK;
+}
+
+}  // namespace
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_error, sizeof(g_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int32_t* status_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int encode_cache_map(CUtensorMap* map, const void* cache, pa_dtype dtype, int num_blocks,
+                     int num_kv_heads, int block_size, int head_dim) {
+  auto enc = encoder();
+  if (enc == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {(cuuint64_t)head_dim,
+                              (cuuint64_t)num_blocks * num_kv_heads * block_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * dtype_bytes(dtype)};
+  const cuuint32_t box[2] = {64, (cuuint32_t)block_size};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, tma_dtype(dtype), 2, const_cast<void*>(cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int encode_query_map(CUtensorMap* map, const void* q, pa_dtype dtype, int num_tokens,
+                     int num_q_heads, int head_dim, int group, int rows_per_box) {
+  auto enc = encoder();
+  if (enc == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const size_t e = dtype_bytes(dtype);
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads,
+                              (cuuint64_t)num_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * e, (cuuint64_t)num_q_heads * head_dim * e};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)rows_per_box};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, tma_dtype(dtype), 3, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_last_error_string(void) { return g_error; }
+
+int pa_get_status(int32_t* status) {
+  g_error[0] = '\0';
+  if (status == nullptr) return fail(PA_ERR_INVALID_ARG, "pa_get_status: null output pointer");
+  int32_t* p = status_word();
+  if (p == nullptr) return fail(PA_ERR_CUDA, "pa_get_status: no usable CUDA device");
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(status, p, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(p, 0, sizeof(int32_t)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return fail(PA_ERR_CUDA, "pa_get_status: %s", cudaGetErrorString(cudaGetLastError()));
+  return PA_OK;
+}
+
+int pa_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                    int num_tokens, int block_size, int num_blocks, void* stream) {
+  g_error[0] = '\0';
+  if (num_seqs < 0 || num_tokens < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_slot_mapping: negative sizes");
+  if (num_tokens == 0) return PA_OK;
+  if (num_seqs == 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_slot_mapping: tokens without sequences or blocks");
+  if (!slots || !block_tables || !cu_q_lens || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "pa_slot_mapping: null pointer");
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_slot_mapping: no usable CUDA device");
+  cudaError_t e = launch_slot_mapping(slots, block_tables, max_blocks_per_seq, cu_q_lens,
+                                      context_lens, num_seqs, num_tokens, block_size, num_blocks,
+                                      st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_slot_mapping: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         void* stream) {
+  g_error[0] = '\0';
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: num_tokens < 0");
+  int rc = check_cache_geometry("pa_reshape_and_cache", num_kv_heads, head_dim, block_size,
+                                num_blocks, dtype);
+  if (rc != PA_OK) return rc;
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: null pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: K/V pointers must be 16-byte aligned");
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_reshape_and_cache: no usable CUDA device");
+  cudaError_t e = launch_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
+                                           num_tokens, num_kv_heads, head_dim, block_size,
+                                           num_blocks, dtype_bytes(dtype), st,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(PA_ERR_CUDA, "pa_reshape_and_cache: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                   const int32_t* pairs, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, pa_dtype dtype, void* stream) {
+  g_error[0] = '\0';
+  if (num_pairs < 0 || num_layers < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: negative sizes");
+  int rc = check_cache_geometry("pa_copy_blocks", num_kv_heads, head_dim, block_size, num_blocks,
+                                dtype);
+  if (rc != PA_OK) return rc;
+  if (num_pairs == 0 || num_layers == 0) return PA_OK;
+  if (num_layers > kMaxCopyLayers)
+    return fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: %d layers > %d", num_layers, kMaxCopyLayers);
+  if (!k_caches || !v_caches || !pairs)
+    return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: null pointer");
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+      return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: layer %d cache pointer null or unaligned",
+                  l);
+  }
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_copy_blocks: no usable CUDA device");
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * dtype_bytes(dtype);
+  cudaError_t e = launch_copy_blocks(k_caches, v_caches, num_layers, pairs, num_pairs,
+                                     block_bytes, num_blocks, st,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_copy_blocks: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_ctx, int block_size) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_ctx < 0 ||
+      block_size <= 0)
+    return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size);
+}
+
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
+              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+              pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  int rc = check_cache_geometry("pa_decode", num_kv_heads, head_dim, block_size, num_blocks,
+                                dtype);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || max_ctx < 0 || num_q_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: negative sizes");
+  if (num_seqs == 0) return PA_OK;
+  if (!valid_dtype(out_dtype) || (out_dtype != dtype && out_dtype != PA_F32))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: out_dtype must equal dtype or be PA_F32");
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: num_q_heads %d not a multiple of num_kv_heads %d",
+                num_q_heads, num_kv_heads);
+  if (!supported_group(num_q_heads / num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: group size %d not built (1, 2, 4, 8, 16)",
+                num_q_heads / num_kv_heads);
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq <= 0");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale is NaN");
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: null pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: out/q/caches/workspace must be 16-byte aligned");
+  const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             max_ctx, block_size);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "pa_decode: workspace %zu bytes < %zu needed", workspace_bytes,
+                need);
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_decode: no usable CUDA device");
+  DecodeArgs a;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_ctx = max_ctx;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.ws = carve_decode_workspace(workspace, num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size);
+  a.status = st;
+  return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int max_ctx, int block_size) {
+  if (num_seqs <= 0 || num_tokens < 0 || max_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || max_ctx < 0 || block_size <= 0)
+    return 0;
+  return prefill_workspace_bytes(num_seqs, num_tokens, max_q, num_q_heads, num_kv_heads, head_dim,
+                                 max_ctx, block_size);
+}
+
+int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                     int num_tokens, int max_q, int max_ctx, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  int rc = check_cache_geometry("pa_prefill_chunk", num_kv_heads, head_dim, block_size,
+                                num_blocks, dtype);
+  if (rc != PA_OK) return rc;
+  if (dtype == PA_F32)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: fp32 runs on decode only (f16/bf16 here)");
+  if (num_seqs < 0 || num_tokens < 0 || max_q < 0 || max_ctx < 0 || num_q_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: negative sizes");
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!valid_dtype(out_dtype) || (out_dtype != dtype && out_dtype != PA_F32))
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: out_dtype must equal dtype or be PA_F32");
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_prefill_chunk: num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
+                num_kv_heads);
+  if (!supported_group(num_q_heads / num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: group size %d not built",
+                num_q_heads / num_kv_heads);
+  if (max_blocks_per_seq <= 0 || max_q <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: max_blocks_per_seq and max_q must be > 0");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: scale is NaN");
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_q_lens || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: null pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: out/q/caches must be 16-byte aligned");
+  const size_t need = prefill_workspace_bytes(num_seqs, num_tokens, max_q, num_q_heads,
+                                              num_kv_heads, head_dim, max_ctx, block_size);
+  if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: workspace null or unaligned");
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "pa_prefill_chunk: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_prefill_chunk: no usable CUDA device");
+  PrefillArgs a;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.cu_q_lens = cu_q_lens;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_q = max_q;
+  a.max_ctx = max_ctx;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.status = st;
+  return launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

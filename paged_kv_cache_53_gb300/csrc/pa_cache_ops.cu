@@ -1,0 +1,138 @@
+// Bit-exact cache operations: slot mapping, cache write (reshape_and_cache) and
+// copy-on-write block copies.  All three are pure data movement bounded by HBM (or, at
+// decode sizes, by launch latency); each thread moves 16-byte vectors.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// One thread per new token.  The token's sequence is found by binary search over
+// cu_q_lens; its position is the matching tail position of the sequence's context.
+__global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
+                                    const int32_t* __restrict__ block_tables, int max_blocks,
+                                    const int32_t* __restrict__ cu_q_lens,
+                                    const int32_t* __restrict__ context_lens, int num_seqs,
+                                    int num_tokens, int block_size, int num_blocks,
+                                    int32_t* status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= num_tokens) return;
+  int lo = 0, hi = num_seqs;  // cu_q_lens[lo] <= t < cu_q_lens[hi] when the input is valid
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu_q_lens + mid) <= t) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int first = __ldg(cu_q_lens + b);
+  const int n_new = __ldg(cu_q_lens + b + 1) - first;
+  const long long pos = (long long)__ldg(context_lens + b) - n_new + (t - first);
+  if (t < first || t - first >= n_new || pos < 0 || pos >= (long long)max_blocks * block_size) {
+    flag_status(status, PA_STATUS_BAD_CONTEXT);
+    slots[t] = -1;
+    return;
+  }
+  const int blk = __ldg(block_tables + (size_t)b * max_blocks + pos / block_size);
+  if (blk < 0 || blk >= num_blocks) {
+    flag_status(status, PA_STATUS_BAD_BLOCK);
+    slots[t] = -1;
+    return;
+  }
+  slots[t] = (int64_t)blk * block_size + pos % block_size;
+}
+
+// One thread per 16-byte chunk of one (token, KV head) row; K and V move together.
+__global__ void reshape_and_cache_kernel(const uint4* __restrict__ k_new,
+                                         const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
+                                         uint4* __restrict__ v_cache,
+                                         const int64_t* __restrict__ slots, int num_tokens,
+                                         int num_kv_heads, int chunks_per_row, int block_size,
+                                         long long num_slots, int32_t* status) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_token = (long long)num_kv_heads * chunks_per_row;
+  if (i >= (long long)num_tokens * per_token) return;
+  const long long t = i / per_token;
+  const int rem = (int)(i - t * per_token);
+  const int h = rem / chunks_per_row;
+  const int c = rem - h * chunks_per_row;
+  const long long slot = __ldg(slots + t);
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (rem == 0) flag_status(status, PA_STATUS_BAD_SLOT);
+    return;
+  }
+  const long long blk = slot / block_size, off = slot - blk * block_size;
+  const long long dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+  const long long src = i;
+  k_cache[dst] = __ldg(k_new + src);
+  v_cache[dst] = __ldg(v_new + src);
+}
+
+struct LayerPtrs {
+  uint4* k[kMaxCopyLayers];
+  uint4* v[kMaxCopyLayers];
+};
+
+// One CTA per (pair, layer, K-or-V); the CTA copies one whole block (all KV heads).
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs,
+                                                          const int32_t* __restrict__ pairs,
+                                                          int chunks_per_block, int num_blocks,
+                                                          int32_t* status) {
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.z == 0) flag_status(status, PA_STATUS_BAD_BLOCK);
+    return;
+  }
+  uint4* base = blockIdx.z == 0 ? ptrs.k[layer] : ptrs.v[layer];
+  const uint4* s = base + (size_t)src * chunks_per_block;
+  uint4* d = base + (size_t)dst * chunks_per_block;
+  for (int c = threadIdx.x; c < chunks_per_block; c += blockDim.x) d[c] = __ldg(s + c);
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                                const int32_t* cu_q_lens, const int32_t* context_lens,
+                                int num_seqs, int num_tokens, int block_size, int num_blocks,
+                                int32_t* status, cudaStream_t stream) {
+  const int threads = 256;
+  slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0, stream>>>(
+      slots, block_tables, max_blocks, cu_q_lens, context_lens, num_seqs, num_tokens, block_size,
+      num_blocks, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int64_t* slots, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int num_blocks, size_t elem_bytes, int32_t* status,
+                                     cudaStream_t stream) {
+  const int chunks_per_row = (int)(head_dim * elem_bytes / 16);
+  const long long total = (long long)num_tokens * num_kv_heads * chunks_per_row;
+  const int threads = 256;
+  const long long grid = (total + threads - 1) / threads;
+  if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+  reshape_and_cache_kernel<<<(unsigned)grid, threads, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads,
+      chunks_per_row, block_size, (long long)num_blocks * block_size, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int32_t* pairs, int num_pairs, size_t block_bytes,
+                               int num_blocks, int32_t* status, cudaStream_t stream) {
+  LayerPtrs ptrs;
+  for (int l = 0; l < num_layers; ++l) {
+    ptrs.k[l] = static_cast<uint4*>(k_caches[l]);
+    ptrs.v[l] = static_cast<uint4*>(v_caches[l]);
+  }
+  for (int l = num_layers; l < kMaxCopyLayers; ++l) ptrs.k[l] = ptrs.v[l] = nullptr;
+  if (num_pairs > 0x7fffffff || num_layers > 65535) return cudaErrorInvalidValue;
+  dim3 grid(num_pairs, num_layers, 2);
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(ptrs, pairs, (int)(block_bytes / 16), num_blocks,
+                                               status);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

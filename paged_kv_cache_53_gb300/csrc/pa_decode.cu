@@ -1,0 +1,842 @@
+// Paged decode attention (one query token per sequence) for sm_103a.
+//
+// Three launches per call, all on the caller's stream:
+//   1. plan   -- one CTA reads the context lengths, picks the split-KV partition size so
+//                that about kTargetUnits (partition, KV head) units exist, and writes the
+//                partition list sorted largest first (longest-processing-time order, so
+//                the dynamic scheduler below ends with the smallest units).
+//   2. attend -- a persistent kernel, one CTA per SM.  Each CTA holds kPairs pairs of
+//                warps; in a pair a producer warp grabs units from a global counter,
+//                reads the unit's block-table entries, and streams every (block, KV
+//                head) K and V tile into a ring of shared-memory stages with TMA; the
+//                consumer warp runs q.K^T and P.V on the tensor cores (mma.sync
+//                m16n8k16, the query group padded to 16 rows) with an online softmax.
+//                A unit covering a whole context writes the normalised output; the
+//                others write an fp32 partial (running max, sum, unnormalised output).
+//   3. merge  -- one CTA per (sequence, KV head) with more than one partition merges the
+//                partials by log-sum-exp rescaling.
+// fp32 caches take a CUDA-core variant of step 2 (tensor cores have no fp32 input path
+// that meets an fp32 tolerance).
+//
+// The decode is bound by HBM: every context token's K and V row is read once and each
+// byte feeds ~1 (MHA) to ~8 (group of 8) flops, far below the ridge point.  The design
+// therefore aims at bytes in flight (up to ~190 KiB of TMA copies per SM) and keeps the
+// per-tile instruction count small.
+#include <algorithm>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+// The running maximum is only moved when a tile's maximum exceeds it by more than this
+// many powers of two; in between, probabilities up to 2^8 are accumulated, which fp32
+// sums and 16-bit hi/lo splits of P represent without loss of accuracy.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+struct DecodeParams {
+  const void* q;
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  DecodeWorkspace ws;
+  int32_t* status;
+  int max_blocks, ctx_cap, num_seqs, num_q_heads, num_kv_heads, group, num_blocks;
+  int out_f32;
+  float scale_log2;
+};
+
+// A unit as the producer hands it to its consumer.
+struct UnitDesc {
+  int b, h, tok0, ntok, nparts, part_idx, valid, pad;
+};
+
+__device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// ----------------------------------------------------------------------------------
+// 1. plan
+// ----------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ context_lens,
+                                                           int num_seqs, int ctx_cap,
+                                                           int num_kv_heads, int block_size,
+                                                           DecodeWorkspace ws, int32_t* status) {
+  __shared__ long long s_sum[32];
+  __shared__ int s_off[32];
+  __shared__ int s_hist[kMaxPartBlocks + 2];
+  __shared__ int s_psz, s_total;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
+  const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+
+  long long sum = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int c = context_lens[b];
+    if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
+    sum += clamp_ctx(c, ctx_cap);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
+  if (lane == 0) s_sum[wid] = sum;
+  for (int i = tid; i < kMaxPartBlocks + 2; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    long long total = 0;
+    for (int w = 0; w < nwarps; ++w) total += s_sum[w];
+    long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
+    want = (want + block_size - 1) / block_size * block_size;
+    want = max(want, (long long)kMinPartBlocks * block_size);
+    want = min(want, (long long)kMaxPartBlocks * block_size);
+    s_psz = (int)want;
+  }
+  __syncthreads();
+  const int psz = s_psz, bpp = psz / block_size;
+
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int c = clamp_ctx(context_lens[b], ctx_cap);
+    const int np = (c + psz - 1) / psz;
+    local += np;
+    if (np > 0) {
+      const int tail = c - (np - 1) * psz;
+      atomicAdd(&s_hist[(tail + block_size - 1) / block_size], 1);
+      if (np > 1) atomicAdd(&s_hist[bpp], np - 1);
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_off[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = lane < nwarps ? s_off[lane] : 0;
+    int iv = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(~0u, iv, o);
+      if (lane >= o) iv += t;
+    }
+    if (lane < nwarps) s_off[lane] = iv - v;
+    if (lane == 31) s_total = iv;
+  }
+  __syncthreads();
+  int run = s_off[wid] + incl - local;
+  for (int b = b0; b < b1; ++b) {
+    ws.part_start[b] = run;
+    run += (clamp_ctx(context_lens[b], ctx_cap) + psz - 1) / psz;
+  }
+  if (tid == 0) {
+    ws.part_start[num_seqs] = s_total;
+    int acc = 0;  // bucket offsets, largest partitions first
+    for (int k = bpp; k >= 1; --k) {
+      const int h = s_hist[k];
+      s_hist[k] = acc;
+      acc += h;
+    }
+  }
+  __syncthreads();
+  for (int b = b0; b < b1; ++b) {
+    const int c = clamp_ctx(context_lens[b], ctx_cap);
+    const int np = (c + psz - 1) / psz;
+    for (int p = 0; p < np; ++p) {
+      const int ntok = min(psz, c - p * psz);
+      const int slot = atomicAdd(&s_hist[(ntok + block_size - 1) / block_size], 1);
+      ws.units[slot] = make_int2(b, p);
+    }
+  }
+  if (tid == 0) {
+    ws.header[0] = 0;
+    ws.header[1] = s_total * num_kv_heads;
+    ws.header[2] = psz;
+    ws.header[3] = s_total;
+  }
+}
+
+// Decodes unit u into its sequence, partition, head and extent.
+__device__ __forceinline__ UnitDesc describe_unit(const DecodeParams& p, int u, int psz) {
+  const int part_global = u / p.num_kv_heads;
+  const int2 bp = p.ws.units[part_global];
+  UnitDesc d;
+  d.b = bp.x;
+  d.h = u - part_global * p.num_kv_heads;
+  d.tok0 = bp.y * psz;
+  const int ctx = clamp_ctx(__ldg(p.context_lens + d.b), p.ctx_cap);
+  d.ntok = min(psz, ctx - d.tok0);
+  const int ps = p.ws.part_start[d.b];
+  d.nparts = p.ws.part_start[d.b + 1] - ps;
+  d.part_idx = ps + bp.y;
+  d.valid = 1;
+  d.pad = 0;
+  return d;
+}
+
+// ----------------------------------------------------------------------------------
+// 2a. attend: TMA + tensor cores (fp16 / bf16)
+// ----------------------------------------------------------------------------------
+template <int D, int BS, int EB>
+struct MmaCfg {
+  static constexpr int kPairs = 4;                       // producer/consumer warp pairs
+  static constexpr int kBoxBytes = BS * 128;             // BS rows x 64 elements (128 B)
+  static constexpr int kHalves = D / 64;                 // boxes per K (or V) tile
+  static constexpr int kTileBytes = kHalves * kBoxBytes;  // one K or V tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRingBytesPerPair = 48 * 1024;
+  static constexpr int kStages =
+      kRingBytesPerPair / kStageBytes > 8 ? 8 : kRingBytesPerPair / kStageBytes;
+  static constexpr int kThreads = 2 * kPairs * 32;
+  static constexpr int kBars = 2 * kPairs * kStages + 4 * kPairs;
+
+  __host__ __device__ static size_t qstride(int group) {
+    return ((size_t)group * D * EB + 127) / 128 * 128;
+  }
+  static size_t smem_bytes(int group) {
+    return 1024 + (size_t)kPairs * kStages * kStageBytes + kPairs * 2 * qstride(group) + 128 +
+           kBars * 8 + kPairs * 2 * sizeof(UnitDesc);
+  }
+};
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+  using C = MmaCfg<D, BS, 2>;
+  using M = Mma<T>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int G = p.group;
+  const uint32_t qstride = (uint32_t)C::qstride(G);
+  uint8_t* stages = base;
+  uint8_t* qbuf = stages + (size_t)C::kPairs * S * C::kStageBytes;
+  uint8_t* zero16 = qbuf + (size_t)C::kPairs * 2 * qstride;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(zero16 + 128);
+  UnitDesc* descs = reinterpret_cast<UnitDesc*>(bars + C::kBars);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp % C::kPairs;
+  uint64_t* full = bars + pair * S;
+  uint64_t* empty = bars + C::kPairs * S + pair * S;
+  uint64_t* qfull = bars + 2 * C::kPairs * S + pair * 2;
+  uint64_t* qempty = bars + 2 * C::kPairs * S + 2 * C::kPairs + pair * 2;
+  UnitDesc* mydesc = descs + pair * 2;
+  uint8_t* myq = qbuf + (size_t)pair * 2 * qstride;
+  uint8_t* mystages = stages + (size_t)pair * S * C::kStageBytes;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kBars; ++i) mbar_init(smem_addr(bars + i), 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(zero16)[threadIdx.x] = 0;
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  __syncthreads();
+
+  const int total_units = p.ws.header[1];
+  const int psz = p.ws.header[2];
+
+  if (warp >= C::kPairs) {
+    // ------------------------------ producer warp ------------------------------
+    const uint32_t qbytes = (uint32_t)G * D * sizeof(T);
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t tile_it = 0, q_it = 0;
+    int next_u = 0;
+    if (lane == 0) next_u = atomicAdd(p.ws.header, 1);
+    next_u = __shfl_sync(~0u, next_u, 0);
+    bool ok = true;
+    while (ok) {
+      const int u = next_u;
+      const int qs = q_it & 1;
+      if (!mbar_wait(smem_addr(qempty + qs), ((q_it >> 1) & 1) ^ 1)) { ok = false; break; }
+      if (u >= total_units) {
+        if (lane == 0) {
+          mydesc[qs].valid = 0;
+          mbar_arrive(smem_addr(qfull + qs));
+        }
+        break;
+      }
+      if (lane == 0) next_u = atomicAdd(p.ws.header, 1);  // fetch the next unit early
+      const UnitDesc d = describe_unit(p, u, psz);
+      const int ntiles = (d.ntok + BS - 1) / BS;
+      const int32_t* row = p.block_tables + (size_t)d.b * p.max_blocks + d.tok0 / BS;
+      int ids[kMaxPartBlocks / 32];
+#pragma unroll
+      for (int k = 0; k < kMaxPartBlocks / 32; ++k) {
+        const int t = lane + 32 * k;
+        int id = -1;
+        if (t < ntiles) {
+          id = __ldg(row + t);
+          if (id < 0 || id >= p.num_blocks) {
+            flag_status(p.status, PA_STATUS_BAD_BLOCK);
+            id = -1;
+          }
+        }
+        ids[k] = id;
+      }
+      if (lane == 0) {
+        mydesc[qs] = d;
+        const uint32_t bar = smem_addr(qfull + qs);
+        mbar_arrive_expect_tx(bar, qbytes);
+        bulk_load(smem_addr(myq + qs * qstride),
+                  static_cast<const T*>(p.q) + ((size_t)d.b * p.num_q_heads + (size_t)d.h * G) * D,
+                  qbytes, bar);
+      }
+      ++q_it;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = tile_it % S;
+        if (!mbar_wait(smem_addr(empty + s), ((tile_it / S) & 1) ^ 1)) { ok = false; break; }
+        const int k = t >> 5;
+        int id = k == 0 ? ids[0] : k == 1 ? ids[1] : k == 2 ? ids[2] : ids[3];
+        id = __shfl_sync(~0u, id, t & 31);
+        if (lane == 0) {
+          // a bad block id reads a box that lies wholly outside the tensor: zeros
+          const int y = id < 0 ? -BS : (id * p.num_kv_heads + d.h) * BS;
+          const uint32_t bar = smem_addr(full + s);
+          mbar_arrive_expect_tx(bar, C::kStageBytes);
+          uint8_t* st = mystages + (size_t)s * C::kStageBytes;
+#pragma unroll
+          for (int hb = 0; hb < C::kHalves; ++hb) {
+            tma_load_2d(smem_addr(st + hb * C::kBoxBytes), &tmk, hb * 64, y, bar, policy);
+            tma_load_2d(smem_addr(st + C::kTileBytes + hb * C::kBoxBytes), &tmv, hb * 64, y, bar,
+                        policy);
+          }
+        }
+        ++tile_it;
+      }
+      next_u = __shfl_sync(~0u, next_u, 0);
+    }
+    if (!ok) {
+      if (lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+      // let copies already issued land before the CTA can exit
+      const uint32_t first = tile_it > (uint32_t)S ? tile_it - S : 0;
+      for (uint32_t i = first; i < tile_it; ++i) mbar_wait(smem_addr(full + i % S), (i / S) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------ consumer warp ------------------------------
+  constexpr int NT = BS / 8;   // 8-token score tiles per K tile
+  constexpr int KS = D / 16;   // k-steps of q.K^T
+  constexpr int ON = D / 8;    // 8-column output tiles
+  const int g0 = lane >> 2, c4 = lane & 3;
+  const bool hi_rows = G > 8;  // rows 8..15 of the padded query group are real
+  const uint32_t zero_addr = smem_addr(zero16);
+  uint32_t tile_it = 0, q_it = 0;
+  for (;;) {
+    const int qs = q_it & 1;
+    if (!mbar_wait(smem_addr(qfull + qs), (q_it >> 1) & 1)) {
+      if (lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+      return;
+    }
+    const UnitDesc d = mydesc[qs];
+    if (!d.valid) return;
+
+    // query group as A fragments (rows >= G read zeros)
+    uint32_t qa[KS][4];
+    {
+      const int i = lane >> 3;
+      const int r = (lane & 7) + 8 * (i & 1);
+      const uint32_t rowbase = smem_addr(myq + qs * qstride) + r * (D * sizeof(T));
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint32_t addr = r < G ? rowbase + (2 * kk + (i >> 1)) * 16 : zero_addr;
+        ldsm_x4(addr, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(qempty + qs));
+    ++q_it;
+
+    float o[ON][4];
+#pragma unroll
+    for (int j = 0; j < ON; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+
+    const int ntiles = (d.ntok + BS - 1) / BS;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = tile_it % S;
+      if (!mbar_wait(smem_addr(full + s), (tile_it / S) & 1)) {
+        if (lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+        return;
+      }
+      const uint32_t kbase = smem_addr(mystages + (size_t)s * C::kStageBytes);
+      const uint32_t vbase = kbase + C::kTileBytes;
+
+      // scores: S[16 x BS] = Qpad[16 x D] . K^T
+      float sc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        const int tok = nt * 8 + (lane & 7);
+#pragma unroll
+        for (int kk2 = 0; kk2 < D / 32; ++kk2) {
+          const int cg = 4 * kk2 + (lane >> 3);
+          const uint32_t addr =
+              kbase + (cg >> 3) * C::kBoxBytes + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          M::run(sc[nt], qa[2 * kk2], b0, b1);
+          M::run(sc[nt], qa[2 * kk2 + 1], b2, b3);
+        }
+      }
+      // scale into log2 units; tokens past the context never count
+      const int limit = d.ntok - t * BS;
+      float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool valid = nt * 8 + 2 * c4 + e < limit;
+          sc[nt][e] = valid ? sc[nt][e] * p.scale_log2 : kNegInf;
+          sc[nt][2 + e] = valid ? sc[nt][2 + e] * p.scale_log2 : kNegInf;
+          mx0 = fmaxf(mx0, sc[nt][e]);
+          mx1 = fmaxf(mx1, sc[nt][2 + e]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, 2));
+      const bool need0 = mx0 > m0 + kRescaleThreshold;
+      const bool need1 = hi_rows && mx1 > m1 + kRescaleThreshold;
+      if (__any_sync(~0u, need0 || need1)) {
+        if (need0) {
+          const float a = fast_exp2(m0 - mx0);
+          m0 = mx0;
+          l0 *= a;
+#pragma unroll
+          for (int j = 0; j < ON; ++j) { o[j][0] *= a; o[j][1] *= a; }
+        }
+        if (need1) {
+          const float a = fast_exp2(m1 - mx1);
+          m1 = mx1;
+          l1 *= a;
+#pragma unroll
+          for (int j = 0; j < ON; ++j) { o[j][2] *= a; o[j][3] *= a; }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sc[nt][0] = fast_exp2(sc[nt][0] - m0);
+        sc[nt][1] = fast_exp2(sc[nt][1] - m0);
+        l0 += sc[nt][0] + sc[nt][1];
+        if (hi_rows) {
+          sc[nt][2] = fast_exp2(sc[nt][2] - m1);
+          sc[nt][3] = fast_exp2(sc[nt][3] - m1);
+          l1 += sc[nt][2] + sc[nt][3];
+        } else {
+          sc[nt][2] = sc[nt][3] = 0.f;
+        }
+      }
+      // O[16 x D] += P[16 x BS] . V, with P carried as hi + lo 16-bit terms
+#pragma unroll
+      for (int ks = 0; ks < BS / 16; ++ks) {
+        uint32_t ah[4], al[4];
+        ah[0] = M::pack_split(sc[2 * ks][0], sc[2 * ks][1], al[0]);
+        ah[1] = M::pack_split(sc[2 * ks][2], sc[2 * ks][3], al[1]);
+        ah[2] = M::pack_split(sc[2 * ks + 1][0], sc[2 * ks + 1][1], al[2]);
+        ah[3] = M::pack_split(sc[2 * ks + 1][2], sc[2 * ks + 1][3], al[3]);
+        const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+        // V rows of tokens past the context may hold anything (even NaN bits) and are
+        // multiplied by P = 0: clear them in the fragments of the last tile.
+        const int vlim = limit - 16 * ks;
+        const bool tail = vlim < 16;
+        const uint32_t m_lo0 = (2 * c4 < vlim ? 0x0000ffffu : 0u) | (2 * c4 + 1 < vlim ? 0xffff0000u : 0u);
+        const uint32_t m_hi0 =
+            (2 * c4 + 8 < vlim ? 0x0000ffffu : 0u) | (2 * c4 + 9 < vlim ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int dt2 = 0; dt2 < D / 16; ++dt2) {
+          const int cg = 2 * dt2 + (lane >> 4);
+          const uint32_t addr =
+              vbase + (cg >> 3) * C::kBoxBytes + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(addr, b0, b1, b2, b3);
+          if (tail) {
+            b0 &= m_lo0;
+            b1 &= m_hi0;
+            b2 &= m_lo0;
+            b3 &= m_hi0;
+          }
+          M::run(o[2 * dt2], ah, b0, b1);
+          M::run(o[2 * dt2], al, b0, b1);
+          M::run(o[2 * dt2 + 1], ah, b2, b3);
+          M::run(o[2 * dt2 + 1], al, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(empty + s));
+      ++tile_it;
+    }
+
+    l0 += __shfl_xor_sync(~0u, l0, 1);
+    l0 += __shfl_xor_sync(~0u, l0, 2);
+    l1 += __shfl_xor_sync(~0u, l1, 1);
+    l1 += __shfl_xor_sync(~0u, l1, 2);
+    const int hq0 = d.h * G;
+    if (d.nparts == 1) {
+      const size_t row0 = ((size_t)d.b * p.num_q_heads + hq0) * D;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int g = g0 + 8 * half;
+        if (g >= G) continue;
+        const float inv = 1.f / (half ? l1 : l0);
+        const size_t at = row0 + (size_t)g * D + 2 * c4;
+        if (p.out_f32) {
+          float* out = static_cast<float*>(p.out) + at;
+#pragma unroll
+          for (int j = 0; j < ON; ++j) store2(out + j * 8, o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
+        } else {
+          T* out = static_cast<T*>(p.out) + at;
+#pragma unroll
+          for (int j = 0; j < ON; ++j) store2(out + j * 8, o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int g = g0 + 8 * half;
+        if (g >= G) continue;
+        const size_t slot = (size_t)d.part_idx * p.num_q_heads + hq0 + g;
+        float* acc = p.ws.part_acc + slot * D + 2 * c4;
+#pragma unroll
+        for (int j = 0; j < ON; ++j) store2(acc + j * 8, o[j][2 * half], o[j][2 * half + 1]);
+        if (c4 == 0) p.ws.part_ml[slot] = make_float2(half ? m1 : m0, half ? l1 : l0);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// 2b. attend: fp32 on CUDA cores (one warp per unit, one token at a time)
+// ----------------------------------------------------------------------------------
+constexpr int kMaxGroup = 16;
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_f32_kernel(const float* __restrict__ k_cache,
+                                                         const float* __restrict__ v_cache,
+                                                         const DecodeParams p, int block_size) {
+  constexpr int V = D / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int total_units = p.ws.header[1];
+  const int psz = p.ws.header[2];
+  for (;;) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.ws.header, 1);
+    u = __shfl_sync(~0u, u, 0);
+    if (u >= total_units) return;
+    const UnitDesc d = describe_unit(p, u, psz);
+    const float* qb = static_cast<const float*>(p.q) + ((size_t)d.b * p.num_q_heads + (size_t)d.h * G) * D;
+    float qv[kMaxGroup][V], acc[kMaxGroup][V], m[kMaxGroup], l[kMaxGroup];
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      m[g] = kNegInf;
+      l[g] = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        qv[g][i] = g < G ? qb[g * D + lane + 32 * i] : 0.f;
+        acc[g][i] = 0.f;
+      }
+    }
+    const int32_t* row = p.block_tables + (size_t)d.b * p.max_blocks;
+    for (int tok = d.tok0; tok < d.tok0 + d.ntok; ++tok) {
+      const int blk = __ldg(row + tok / block_size);
+      if (blk < 0 || blk >= p.num_blocks) {
+        if (lane == 0) flag_status(p.status, PA_STATUS_BAD_BLOCK);
+        continue;
+      }
+      const size_t off = (((size_t)blk * p.num_kv_heads + d.h) * block_size + tok % block_size) * D;
+      float kv[V], vv[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        kv[i] = __ldg(k_cache + off + lane + 32 * i);
+        vv[i] = __ldg(v_cache + off + lane + 32 * i);
+      }
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        if (g >= G) break;
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) s = fmaf(qv[g][i], kv[i], s);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(~0u, s, o);
+        const float x = s * p.scale_log2;
+        const float mn = fmaxf(m[g], x);
+        const float a = fast_exp2(m[g] - mn);
+        const float e = fast_exp2(x - mn);
+        l[g] = l[g] * a + e;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[g][i] = fmaf(acc[g][i], a, e * vv[i]);
+        m[g] = mn;
+      }
+    }
+    const int hq0 = d.h * G;
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      if (g >= G) break;
+      if (d.nparts == 1) {
+        float* out = static_cast<float*>(p.out) + ((size_t)d.b * p.num_q_heads + hq0 + g) * D;
+        const float inv = 1.f / l[g];
+#pragma unroll
+        for (int i = 0; i < V; ++i) out[lane + 32 * i] = acc[g][i] * inv;
+      } else {
+        const size_t slot = (size_t)d.part_idx * p.num_q_heads + hq0 + g;
+#pragma unroll
+        for (int i = 0; i < V; ++i) p.ws.part_acc[slot * D + lane + 32 * i] = acc[g][i];
+        if (lane == 0) p.ws.part_ml[slot] = make_float2(m[g], l[g]);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// 3. merge partitions: out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
+// ----------------------------------------------------------------------------------
+constexpr int kMergeThreads = 128;
+constexpr int kMergeChunk = 1024;
+
+template <typename TO>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeWorkspace ws, TO* out,
+                                                                     int num_q_heads,
+                                                                     int num_kv_heads, int D) {
+  __shared__ float s_w[kMergeChunk];
+  __shared__ float s_red[kMergeThreads / 32];
+  __shared__ float s_acc[kMergeThreads];
+  const int b = blockIdx.y, h = blockIdx.x;
+  const int G = num_q_heads / num_kv_heads;
+  const int ps = ws.part_start[b];
+  const int np = ws.part_start[b + 1] - ps;
+  if (np == 1) return;  // written directly by the attention kernel
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int slices = kMergeThreads / D;  // 1 or 2
+  const int slice = tid / D, d = tid - slice * D;
+  for (int g = 0; g < G; ++g) {
+    const int hq = h * G + g;
+    TO* o = out + ((size_t)b * num_q_heads + hq) * D;
+    if (np == 0) {
+      for (int i = tid; i < D; i += kMergeThreads) store1(o + i, 0.f);
+      continue;
+    }
+    float mx = kNegInf;
+    for (int i = tid; i < np; i += kMergeThreads)
+      mx = fmaxf(mx, ws.part_ml[(size_t)(ps + i) * num_q_heads + hq].x);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
+    __syncthreads();
+    if (lane == 0) s_red[wid] = mx;
+    __syncthreads();
+    mx = s_red[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, s_red[w]);
+
+    float acc = 0.f, lsum = 0.f;
+    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
+      const int n = min(kMergeChunk, np - c0);
+      __syncthreads();
+      for (int i = tid; i < n; i += kMergeThreads) {
+        const float2 ml = ws.part_ml[(size_t)(ps + c0 + i) * num_q_heads + hq];
+        const float w = fast_exp2(ml.x - mx);
+        s_w[i] = w;
+        lsum += w * ml.y;
+      }
+      __syncthreads();
+      if (slice < slices)
+        for (int i = slice; i < n; i += slices)
+          acc += s_w[i] * ws.part_acc[((size_t)(ps + c0 + i) * num_q_heads + hq) * D + d];
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(~0u, lsum, off);
+    __syncthreads();
+    if (lane == 0) s_red[wid] = lsum;
+    s_acc[tid] = acc;
+    __syncthreads();
+    float L = 0.f;
+    for (int w = 0; w < kMergeThreads / 32; ++w) L += s_red[w];
+    if (slice == 0) {
+      float a = s_acc[tid];
+      for (int sl = 1; sl < slices; ++sl) a += s_acc[tid + sl * D];
+      store1(o + d, a / L);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------------
+constexpr int kMaxDev = 64;
+
+struct KernelSlot {
+  const void* fn;
+  size_t smem_max;
+  int occupancy[kMaxDev];
+  bool configured[kMaxDev];
+};
+
+std::mutex g_cfg_mutex;
+
+// Sets the kernel's shared-memory limit and reads its occupancy once per device.
+int configure(KernelSlot& k, int dev, int threads, size_t smem_launch) {
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  if (!k.configured[dev]) {
+    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)k.smem_max) != cudaSuccess)
+      return -1;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.fn, threads, k.smem_max) !=
+        cudaSuccess)
+      return -1;
+    k.occupancy[dev] = occ < 1 ? 1 : occ;
+    k.configured[dev] = true;
+  }
+  (void)smem_launch;
+  return k.occupancy[dev];
+}
+
+template <typename T, int D, int BS>
+KernelSlot& mma_slot() {
+  static KernelSlot slot = {reinterpret_cast<const void*>(&decode_mma_kernel<T, D, BS>),
+                            MmaCfg<D, BS, 2>::smem_bytes(kMaxGroup), {}, {}};
+  return slot;
+}
+
+template <typename T, int D, int BS>
+int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
+  using C = MmaCfg<D, BS, 2>;
+  CUtensorMap tmk, tmv;
+  int r1 = encode_cache_map(&tmk, a.k_cache, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
+                            a.head_dim);
+  int r2 = encode_cache_map(&tmv, a.v_cache, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
+                            a.head_dim);
+  if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS)
+    return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed (%d, %d)", r1, r2);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  KernelSlot& slot = mma_slot<T, D, BS>();
+  const int occ = configure(slot, dev, C::kThreads, slot.smem_max);
+  if (occ < 0) return fail(PA_ERR_CUDA, "pa_decode: kernel configuration failed");
+  const int grid = sm_count() * occ;
+  decode_mma_kernel<T, D, BS><<<grid, C::kThreads, C::smem_bytes(p.group), stream>>>(tmk, tmv, p);
+  return PA_OK;
+}
+
+template <typename T>
+int launch_mma_dispatch(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
+  if (a.head_dim == 128 && a.block_size == 16) return launch_mma<T, 128, 16>(a, p, stream);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_mma<T, 128, 32>(a, p, stream);
+  if (a.head_dim == 64 && a.block_size == 16) return launch_mma<T, 64, 16>(a, p, stream);
+  if (a.head_dim == 64 && a.block_size == 32) return launch_mma<T, 64, 32>(a, p, stream);
+  return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim %d / block_size %d", a.head_dim,
+              a.block_size);
+}
+
+}  // namespace
+
+size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size) {
+  const long long pmax = (long long)kMaxPartBlocks * block_size;
+  const long long by_target = (kTargetUnits + num_kv_heads - 1) / num_kv_heads;
+  const long long by_length = (long long)num_seqs * ((max_ctx + pmax - 1) / pmax);
+  return (size_t)(std::max(by_target, by_length) + num_seqs);
+}
+
+namespace {
+struct WsLayout {
+  size_t header, part_start, units, part_ml, part_acc, total;
+};
+WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
+                       int block_size) {
+  const size_t parts = decode_max_parts(num_seqs, num_kv_heads, max_ctx, block_size);
+  WsLayout l;
+  l.header = 0;
+  l.part_start = 256;
+  l.units = align_up(l.part_start + sizeof(int) * (num_seqs + 1), 256);
+  l.part_ml = align_up(l.units + sizeof(int2) * parts, 256);
+  l.part_acc = align_up(l.part_ml + sizeof(float2) * parts * num_q_heads, 256);
+  l.total = align_up(l.part_acc + sizeof(float) * parts * num_q_heads * head_dim, 256);
+  return l;
+}
+}  // namespace
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int max_ctx, int block_size) {
+  return decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size).total;
+}
+
+DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int max_ctx, int block_size) {
+  const WsLayout l =
+      decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  DecodeWorkspace w;
+  w.header = reinterpret_cast<int*>(b + l.header);
+  w.part_start = reinterpret_cast<int*>(b + l.part_start);
+  w.units = reinterpret_cast<int2*>(b + l.units);
+  w.part_ml = reinterpret_cast<float2*>(b + l.part_ml);
+  w.part_acc = reinterpret_cast<float*>(b + l.part_acc);
+  return w;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "pa_decode: more than 65535 sequences");
+  const long long cap = std::min<long long>(a.max_ctx, (long long)a.max_blocks * a.block_size);
+  const int ctx_cap = (int)std::min<long long>(cap, 0x7fffffffll);
+
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, ctx_cap, a.num_kv_heads,
+                                             a.block_size, a.ws, a.status);
+  DecodeParams p;
+  p.q = a.q;
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.ws = a.ws;
+  p.status = a.status;
+  p.max_blocks = a.max_blocks;
+  p.ctx_cap = ctx_cap;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.num_blocks = a.num_blocks;
+  p.out_f32 = a.out_dtype == PA_F32 && a.dtype != PA_F32;
+  p.scale_log2 = a.scale * kLog2e;
+
+  int rc = PA_OK;
+  if (a.dtype == PA_F32) {
+    const int grid = std::max(1, sm_count()) * 8;
+    if (a.head_dim == 128)
+      decode_f32_kernel<128><<<grid, 128, 0, stream>>>(static_cast<const float*>(a.k_cache),
+                                                       static_cast<const float*>(a.v_cache), p,
+                                                       a.block_size);
+    else
+      decode_f32_kernel<64><<<grid, 128, 0, stream>>>(static_cast<const float*>(a.k_cache),
+                                                      static_cast<const float*>(a.v_cache), p,
+                                                      a.block_size);
+  } else if (a.dtype == PA_BF16) {
+    rc = launch_mma_dispatch<__nv_bfloat16>(a, p, stream);
+  } else {
+    rc = launch_mma_dispatch<__half>(a, p, stream);
+  }
+  if (rc != PA_OK) return rc;
+
+  dim3 grid(a.num_kv_heads, a.num_seqs);
+  if (a.out_dtype == PA_F32)
+    decode_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(
+        a.ws, static_cast<float*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
+  else if (a.out_dtype == PA_BF16)
+    decode_merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(
+        a.ws, static_cast<__nv_bfloat16*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
+  else
+    decode_merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(
+        a.ws, static_cast<__half*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+}  // namespace pa

@@ -1,0 +1,130 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Records a failure for pa_last_error_string() and returns `code`.
+int fail(int code, const char* fmt, ...);
+
+// Device address of the current device's status word (nullptr if unavailable).
+int32_t* status_word();
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Encodes a 2-D TMA descriptor over a K or V cache viewed as rows of head_dim elements
+// ([num_blocks * num_kv_heads * block_size, head_dim]); each box is block_size rows by
+// 64 elements with the 128-byte swizzle.  Returns a CUresult.
+int encode_cache_map(CUtensorMap* map, const void* cache, pa_dtype dtype, int num_blocks,
+                     int num_kv_heads, int block_size, int head_dim);
+
+// Encodes a 3-D TMA descriptor over query rows [tokens, num_q_heads, head_dim] for one
+// KV head's group: box = 64 elements x group heads x rows_per_box tokens.
+int encode_query_map(CUtensorMap* map, const void* q, pa_dtype dtype, int num_tokens,
+                     int num_q_heads, int head_dim, int group, int rows_per_box);
+
+inline size_t dtype_bytes(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------------------------
+// cache operations (pa_cache_ops.cu)
+// ----------------------------------------------------------------------------------
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                                const int32_t* cu_q_lens, const int32_t* context_lens,
+                                int num_seqs, int num_tokens, int block_size, int num_blocks,
+                                int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int64_t* slots, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int num_blocks, size_t elem_bytes, int32_t* status,
+                                     cudaStream_t stream);
+
+constexpr int kMaxCopyLayers = 256;
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int32_t* pairs, int num_pairs, size_t block_bytes,
+                               int num_blocks, int32_t* status, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------------
+// decode (pa_decode.cu)
+// ----------------------------------------------------------------------------------
+
+// Split-KV work planning.  A sequence's context is cut into partitions of
+// `part_tokens` tokens (a multiple of the block size, chosen on the device from the
+// batch's total context so that about kTargetUnits (partition, KV head) units exist);
+// partial results of multi-partition sequences are merged by a second kernel.
+constexpr int kTargetUnits = 4096;
+constexpr int kMinPartBlocks = 2;
+constexpr int kMaxPartBlocks = 128;
+
+struct DecodeWorkspace {
+  int* header;        // [0] unit counter, [1] units, [2] part_tokens, [3] partitions
+  int* part_start;    // [num_seqs + 1] first partition index of each sequence
+  int2* units;        // [max_parts] (seq, partition), largest first
+  float2* part_ml;    // [max_parts * num_q_heads] (running max in log2 units, sum)
+  float* part_acc;    // [max_parts * num_q_heads * head_dim] unnormalised outputs
+};
+
+size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int max_ctx, int block_size);
+DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int max_ctx,
+                                       int block_size);
+
+struct DecodeArgs {
+  void* out;
+  pa_dtype out_dtype;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* context_lens;
+  int max_ctx;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+  float scale;
+  pa_dtype dtype;
+  DecodeWorkspace ws;
+  int32_t* status;
+};
+
+// Launches plan + attention + merge kernels.  Returns PA_OK or a PA_ERR_* code (after
+// recording the reason).
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------------
+// chunked prefill (pa_prefill.cu)
+// ----------------------------------------------------------------------------------
+struct PrefillArgs {
+  void* out;
+  pa_dtype out_dtype;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* cu_q_lens;
+  const int32_t* context_lens;
+  int num_seqs, num_tokens, max_q, max_ctx;
+  int num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+  float scale;
+  pa_dtype dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status;
+};
+
+size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int num_q_heads,
+                               int num_kv_heads, int head_dim, int max_ctx, int block_size);
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace pa

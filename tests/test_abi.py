@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads, exports what include/pa.h declares, and rejects bad
+arguments on the host before anything reaches a GPU.
+
+Every call below fails validation, so no kernel is launched and no device memory is
+touched; the pointers passed are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_53_gb300 import build
+    path = build.build()
+    import paged_kv_cache_53_gb300 as pa
+    return pa.lib(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks",
+               "pa_slot_mapping"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.pa_version() >= 100
+
+
+def _err(lib):
+    return lib.pa_last_error_string().decode()
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, out_dtype=2, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxblk=8, ctx=FAKE,
+             max_ctx=128, B=4, Hq=32, Hkv=8, D=128, BS=16, NB=64, scale=0.1, dt=2, ws=FAKE,
+             ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.pa_decode(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["bt"], a["maxblk"],
+                         a["ctx"], a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["BS"],
+                         a["NB"], a["scale"], a["dt"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(D=96), 2, "head_dim"),
+    (dict(BS=8), 2, "block_size"),
+    (dict(Hq=30), 1, "multiple"),
+    (dict(Hq=256, Hkv=8), 2, "group"),
+    (dict(dt=7), 1, "dtype"),
+    (dict(out_dtype=1), 1, "out_dtype"),
+    (dict(q=None), 1, "null"),
+    (dict(k=FAKE + 4), 1, "aligned"),
+    (dict(ws_bytes=16), 3, "workspace"),
+    (dict(maxblk=0), 1, "max_blocks"),
+    (dict(NB=0), 1, "positive"),
+    (dict(scale=float("nan")), 1, "NaN"),
+    (dict(NB=1 << 27, Hkv=8, BS=32), 1, "2^31"),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code, needle):
+    assert _decode(lib, **kw) == code
+    assert needle in _err(lib)
+
+
+def test_zero_sequences_is_a_no_op(lib):
+    assert _decode(lib, B=0, out=None, q=None) == 0
+
+
+def test_workspace_bytes_grow_with_context(lib):
+    f = lib.pa_decode_workspace_bytes
+    small = f(256, 32, 8, 128, 8192, 16)
+    big = f(256, 32, 8, 128, 131072, 16)
+    assert 0 < small < big
+    assert f(0, 32, 8, 128, 10, 16) == 0
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    args = [FAKE, 2, FAKE, FAKE, FAKE, FAKE, 8, FAKE, FAKE, 2, 16, 8, 128, 32, 8, 128, 16, 64,
+            0.1, 0, None, 0, None]  # dtype fp32
+    assert lib.pa_prefill_chunk(*args) == 2 and "fp32" in _err(lib)
+    args[19] = 2   # bf16
+    args[13] = 30  # 30 query heads over 8 KV heads
+    assert lib.pa_prefill_chunk(*args) == 1
+
+
+def test_cache_ops_reject_bad_arguments(lib):
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 100, 16, 64, 2, None) == 2
+    assert lib.pa_reshape_and_cache(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 8, 128, 16, 64, 2,
+                                    None) == 1
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    assert lib.pa_copy_blocks(arr, arr, 300, FAKE, 4, 8, 128, 16, 64, 2, None) == 2
+    assert lib.pa_slot_mapping(FAKE, None, 8, FAKE, FAKE, 4, 4, 16, 64, None) == 1
+    assert lib.pa_slot_mapping(None, None, 8, None, None, 4, 0, 16, 64, None) == 0
+
+
+def test_get_status_without_output_pointer(lib):
+    assert lib.pa_get_status(None) == 1
