@@ -21,7 +21,8 @@
  * Memory.  Every pointer argument named *_cache, q, out, k_new, v_new, block_tables,
  *   context_lens, cu_q_lens, slot_mapping, pairs and workspace is a DEVICE pointer
  *   owned by the caller and must be 16-byte aligned.  The library allocates no device
- *   memory and keeps no state between calls except a per-device status word.
+ *   memory and keeps no state between calls except a per-device status word (and the
+ *   fixed scratch array of pa_decode_static_scratch).
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
  *   enqueues work on it and returns without synchronising.
  * Errors.  A call returns PA_OK or a PA_ERR_* code.  Arguments are validated on the
@@ -159,6 +160,36 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
               pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_static_scratch -- pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for integration.  A caller that
+ * has handed all of the GPU's memory to its own pool (a serving engine typically sizes
+ * its KV-block pool to fill the device) or that must not call cudaMalloc/cudaFree on its
+ * path (they can synchronise the device) has no workspace to pass.  This call takes the
+ * same arguments as pa_decode minus the workspace and computes the same result, using a
+ * 32 MiB array compiled into the library as its scratch.  It allocates nothing.
+ *
+ *   Limit.   Sizes whose pa_decode_workspace_bytes(...) exceeds 32 MiB are rejected
+ *            with PA_ERR_WORKSPACE before anything is launched (for example 256
+ *            sequences of up to 8192 tokens with 32 query heads of 128 fit; 248
+ *            sequences of up to 131072 tokens do not).
+ *   Memory.  Every GPU that loads the library reserves the 32 MiB until the process
+ *            exits.  The first call on each device looks up the array's device address
+ *            (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Sharing. All calls on a device share the one array and it keeps the last call's
+ *            contents; each call rewrites what it reads, so nothing has to be cleared
+ *            between calls.  Calls that overlap in time on the GPU (different streams,
+ *            or different host threads) race on the array and give wrong results:
+ *            serialise them.
+ */
+int pa_decode_static_scratch(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_tables,
+                             int max_blocks_per_seq, const int32_t* context_lens, int max_ctx,
+                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, float scale, pa_dtype dtype,
+                             void* stream);
 
 /*
  * pa_prefill_workspace_bytes -- bytes of device workspace pa_prefill_chunk needs.

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpagedattn.so")
-SOURCES = ["pa_api.cu", "pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu"]
+SOURCES = ["pa_api.cu", "pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu",
+           "pa_decode_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
