@@ -3,41 +3,47 @@
 // decode sizes, by launch latency); each thread moves 16-byte vectors.
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_launch.h"
 
 namespace pa {
 namespace {
 
-// One thread per new token.  The token's sequence is found by binary search over
-// cu_q_lens; its position is the matching tail position of the sequence's context.
-__global__ void slot_mapping_kernel(int64_t* __restrict__ slots,
-                                    const int32_t* __restrict__ block_tables, int max_blocks,
-                                    const int32_t* __restrict__ cu_q_lens,
-                                    const int32_t* __restrict__ context_lens, int num_seqs,
-                                    int num_tokens, int block_size, int num_blocks,
-                                    int32_t* status) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= num_tokens) return;
-  int lo = 0, hi = num_seqs;  // cu_q_lens[lo] <= t < cu_q_lens[hi] when the input is valid
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu_q_lens + mid) <= t) lo = mid; else hi = mid;
-  }
-  const int b = lo;
+// One warp per sequence; its lanes walk the sequence's new tokens.  Token t of
+// sequence b (cu_q_lens[b] <= t < cu_q_lens[b+1]) is the matching tail position of the
+// sequence's context.
+__global__ void __launch_bounds__(256) slot_mapping_kernel(
+    int64_t* __restrict__ slots, const int32_t* __restrict__ block_tables, int max_blocks,
+    const int32_t* __restrict__ cu_q_lens, const int32_t* __restrict__ context_lens,
+    int num_seqs, int num_tokens, int block_size, int num_blocks, int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= num_seqs) return;
   const int first = __ldg(cu_q_lens + b);
   const int n_new = __ldg(cu_q_lens + b + 1) - first;
-  const long long pos = (long long)__ldg(context_lens + b) - n_new + (t - first);
-  if (t < first || t - first >= n_new || pos < 0 || pos >= (long long)max_blocks * block_size) {
-    flag_status(status, PA_STATUS_BAD_CONTEXT);
-    slots[t] = -1;
-    return;
+  const long long ctx = __ldg(context_lens + b);
+  const int32_t* row = block_tables + (size_t)b * max_blocks;
+  for (int i = lane; i < n_new; i += 32) {
+    const long long t = (long long)first + i;
+    if (t < 0 || t >= num_tokens) {
+      flag_status(status, PA_STATUS_BAD_CONTEXT);
+      continue;
+    }
+    const long long pos = ctx - n_new + i;
+    if (pos < 0 || pos >= (long long)max_blocks * block_size) {
+      flag_status(status, PA_STATUS_BAD_CONTEXT);
+      slots[t] = -1;
+      continue;
+    }
+    const int blk = __ldg(row + pos / block_size);
+    if (blk < 0 || blk >= num_blocks) {
+      flag_status(status, PA_STATUS_BAD_BLOCK);
+      slots[t] = -1;
+      continue;
+    }
+    slots[t] = (int64_t)blk * block_size + pos % block_size;
   }
-  const int blk = __ldg(block_tables + (size_t)b * max_blocks + pos / block_size);
-  if (blk < 0 || blk >= num_blocks) {
-    flag_status(status, PA_STATUS_BAD_BLOCK);
-    slots[t] = -1;
-    return;
-  }
-  slots[t] = (int64_t)blk * block_size + pos % block_size;
 }
 
 // One thread per 16-byte chunk of one (token, KV head) row; K and V move together.
@@ -47,6 +53,8 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k_new,
                                          const int64_t* __restrict__ slots, int num_tokens,
                                          int num_kv_heads, int chunks_per_row, int block_size,
                                          long long num_slots, int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_token = (long long)num_kv_heads * chunks_per_row;
   if (i >= (long long)num_tokens * per_token) return;
@@ -77,6 +85,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant_
                                                           const int32_t* __restrict__ pairs,
                                                           int chunks_per_block, int num_blocks,
                                                           int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int pair = blockIdx.x, layer = blockIdx.y;
   const int src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -95,11 +105,10 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int
                                 const int32_t* cu_q_lens, const int32_t* context_lens,
                                 int num_seqs, int num_tokens, int block_size, int num_blocks,
                                 int32_t* status, cudaStream_t stream) {
-  const int threads = 256;
-  slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0, stream>>>(
-      slots, block_tables, max_blocks, cu_q_lens, context_lens, num_seqs, num_tokens, block_size,
-      num_blocks, status);
-  return cudaGetLastError();
+  const int warps_per_cta = 8;
+  return launch_pdl(slot_mapping_kernel, dim3((num_seqs + warps_per_cta - 1) / warps_per_cta),
+                    dim3(32 * warps_per_cta), 0, stream, slots, block_tables, max_blocks,
+                    cu_q_lens, context_lens, num_seqs, num_tokens, block_size, num_blocks, status);
 }
 
 cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
@@ -112,11 +121,11 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void*
   const int threads = 256;
   const long long grid = (total + threads - 1) / threads;
   if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
-  reshape_and_cache_kernel<<<(unsigned)grid, threads, 0, stream>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads,
-      chunks_per_row, block_size, (long long)num_blocks * block_size, status);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)grid), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots,
+                    num_tokens, num_kv_heads, chunks_per_row, block_size,
+                    (long long)num_blocks * block_size, status);
 }
 
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
@@ -129,10 +138,8 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
   }
   for (int l = num_layers; l < kMaxCopyLayers; ++l) ptrs.k[l] = ptrs.v[l] = nullptr;
   if (num_pairs > 0x7fffffff || num_layers > 65535) return cudaErrorInvalidValue;
-  dim3 grid(num_pairs, num_layers, 2);
-  copy_blocks_kernel<<<grid, 256, 0, stream>>>(ptrs, pairs, (int)(block_bytes / 16), num_blocks,
-                                               status);
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, dim3(num_pairs, num_layers, 2), dim3(256), 0, stream, ptrs,
+                    pairs, (int)(block_bytes / 16), num_blocks, status);
 }
 
 }  // namespace pa

@@ -1,10 +1,12 @@
 // Paged decode attention (one query token per sequence) for sm_103a.
 //
-// Three launches per call, all on the caller's stream:
+// Three launches per call on the caller's stream, chained with programmatic dependent
+// launch so that each one's set-up overlaps the previous one:
 //   1. plan   -- one CTA reads the context lengths, picks the split-KV partition size so
 //                that about kTargetUnits (partition, KV head) units exist, and writes the
 //                partition list sorted largest first (longest-processing-time order, so
-//                the dynamic scheduler below ends with the smallest units).
+//                the dynamic scheduler below ends with the smallest units).  It also
+//                zeroes the outputs of empty contexts.
 //   2. attend -- a persistent kernel, one CTA per SM.  Each CTA holds kPairs pairs of
 //                warps; in a pair a producer warp grabs units from a global counter,
 //                reads the unit's block-table entries, and streams every (block, KV
@@ -13,8 +15,11 @@
 //                m16n8k16, the query group padded to 16 rows) with an online softmax.
 //                A unit covering a whole context writes the normalised output; the
 //                others write an fp32 partial (running max, sum, unnormalised output).
-//   3. merge  -- one CTA per (sequence, KV head) with more than one partition merges the
-//                partials by log-sum-exp rescaling.
+//   3. merge  -- one warp per (sequence, KV head) with more than one partition merges
+//                its partials by log-sum-exp rescaling.  (Merging inside the attention
+//                kernel, by whichever warp finished last, stalled that warp's pipeline
+//                on a device-wide fence and an atomic round trip per partition, which
+//                cost more than this launch.)
 // fp32 caches take a CUDA-core variant of step 2 (tensor cores have no fp32 input path
 // that meets an fp32 tolerance).
 //
@@ -27,6 +32,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_launch.h"
 
 namespace pa {
 namespace {
@@ -46,13 +52,15 @@ struct DecodeParams {
   DecodeWorkspace ws;
   int32_t* status;
   int max_blocks, ctx_cap, num_seqs, num_q_heads, num_kv_heads, group, num_blocks;
-  int out_f32;
+  int out_f32;     // fp32 output from 16-bit inputs
+  int out_bytes;   // bytes per output element
+  int out_bf16;    // output is bf16
   float scale_log2;
 };
 
 // A unit as the producer hands it to its consumer.
 struct UnitDesc {
-  int b, h, tok0, ntok, nparts, part_idx, valid, pad;
+  int b, h, tok0, ntok, nparts, part_idx, part_start, valid;
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
@@ -63,7 +71,10 @@ __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ context_lens,
                                                            int num_seqs, int ctx_cap,
                                                            int num_kv_heads, int block_size,
-                                                           DecodeWorkspace ws, int32_t* status) {
+                                                           DecodeWorkspace ws, int32_t* status,
+                                                           int4* out, int out_row_vec16) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ long long s_sum[32];
   __shared__ int s_off[32];
   __shared__ int s_hist[kMaxPartBlocks + 2];
@@ -77,6 +88,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     const int c = context_lens[b];
     if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
     sum += clamp_ctx(c, ctx_cap);
+    if (clamp_ctx(c, ctx_cap) == 0)  // an empty context attends to nothing: zeros
+      for (int i = 0; i < out_row_vec16; ++i) out[(size_t)b * out_row_vec16 + i] = make_int4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
@@ -141,14 +154,24 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     }
   }
   __syncthreads();
+  run = s_off[wid] + incl - local;
   for (int b = b0; b < b1; ++b) {
     const int c = clamp_ctx(context_lens[b], ctx_cap);
     const int np = (c + psz - 1) / psz;
     for (int p = 0; p < np; ++p) {
       const int ntok = min(psz, c - p * psz);
       const int slot = atomicAdd(&s_hist[(ntok + block_size - 1) / block_size], 1);
-      ws.units[slot] = make_int2(b, p);
+      PartRec r;
+      r.b = b;
+      r.p = p;
+      r.tok0 = p * psz;
+      r.ntok = ntok;
+      r.part_start = run;
+      r.nparts = np;
+      r.pad0 = r.pad1 = 0;
+      ws.parts[slot] = r;
     }
+    run += np;
   }
   if (tid == 0) {
     ws.header[0] = 0;
@@ -158,22 +181,146 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   }
 }
 
-// Decodes unit u into its sequence, partition, head and extent.
-__device__ __forceinline__ UnitDesc describe_unit(const DecodeParams& p, int u, int psz) {
-  const int part_global = u / p.num_kv_heads;
-  const int2 bp = p.ws.units[part_global];
+// A unit is (partition, KV head): unit u is partition u / H_kv for KV head u % H_kv.
+__device__ __forceinline__ PartRec load_part(const DecodeParams& p, int u) {
+  const int4* src = reinterpret_cast<const int4*>(p.ws.parts + u / p.num_kv_heads);
+  const int4 a = __ldg(src), c = __ldg(src + 1);
+  PartRec r;
+  r.b = a.x; r.p = a.y; r.tok0 = a.z; r.ntok = a.w;
+  r.part_start = c.x; r.nparts = c.y; r.pad0 = c.z; r.pad1 = c.w;
+  return r;
+}
+
+__device__ __forceinline__ UnitDesc describe_unit(const PartRec& r, int u, int num_kv_heads) {
   UnitDesc d;
-  d.b = bp.x;
-  d.h = u - part_global * p.num_kv_heads;
-  d.tok0 = bp.y * psz;
-  const int ctx = clamp_ctx(__ldg(p.context_lens + d.b), p.ctx_cap);
-  d.ntok = min(psz, ctx - d.tok0);
-  const int ps = p.ws.part_start[d.b];
-  d.nparts = p.ws.part_start[d.b + 1] - ps;
-  d.part_idx = ps + bp.y;
+  d.b = r.b;
+  d.h = u % num_kv_heads;
+  d.tok0 = r.tok0;
+  d.ntok = r.ntok;
+  d.nparts = r.nparts;
+  d.part_idx = r.part_start + r.p;
+  d.part_start = r.part_start;
   d.valid = 1;
-  d.pad = 0;
   return d;
+}
+
+// Combines two (max, sum) pairs of the same row in log2 units.
+__device__ __forceinline__ void combine_ml(float& m, float& l, float m2, float l2) {
+  const float mx = fmaxf(m, m2);
+  if (mx == kNegInf) return;  // both empty
+  l = l * fast_exp2(m - mx) + l2 * fast_exp2(m2 - mx);
+  m = mx;
+}
+
+constexpr int kMaxGroup = 16;
+
+// Merges the partials of one (sequence, KV head) once all of them are written:
+// out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p with M = max_p m_p.  Run by one
+// warp; each lane owns D/32 consecutive columns.  Two dependent rounds of loads: the
+// (max, sum) of every partition and group row, then every partial output row; the rows
+// of all partitions are in flight together.  Partials written by other CTAs are read
+// through L2 (ld.global.cg).
+template <int D, typename TO>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, const UnitDesc& d, TO* out,
+                                               int lane) {
+  constexpr int C = D / 32;
+  const int G = p.group;
+  const int np = d.nparts;
+  const size_t hs = (size_t)p.num_q_heads;
+  const int hq0 = d.h * G;
+  const float2* ml = p.ws.part_ml + (size_t)d.part_start * hs + hq0;  // [partition][g]
+  const float* acc_base = p.ws.part_acc + ((size_t)d.part_start * hs + hq0) * D + lane * C;
+  float M[kMaxGroup], L[kMaxGroup], m_own[kMaxGroup];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    M[g] = kNegInf;
+    L[g] = 0.f;
+    m_own[g] = kNegInf;
+  }
+  // round 1: lane i folds partitions i, i + 32, ... of every row into (max, sum)
+  for (int i0 = 0; i0 < np; i0 += 32) {
+    const int i = i0 + lane;
+    if (i < np) {
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        if (g >= G) break;
+        const float2 v = __ldcg(ml + i * hs + g);
+        if (i0 == 0) m_own[g] = v.x;
+        combine_ml(M[g], L[g], v.x, v.y);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g >= G) break;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(~0u, M[g], o);
+      const float l2 = __shfl_xor_sync(~0u, L[g], o);
+      combine_ml(M[g], L[g], m2, l2);
+    }
+  }
+  // round 2: weighted sum of the partial outputs
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    float mg = 0.f, own = kNegInf;
+#pragma unroll
+    for (int k = 0; k < kMaxGroup; ++k)
+      if (k == g) { mg = M[k]; own = m_own[k]; }
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    for (int i0 = 0; i0 < np; i0 += 32) {
+      const int i = i0 + lane;
+      float w = 0.f;
+      if (i < np) w = fast_exp2((i0 == 0 ? own : __ldcg(ml + i * hs + g).x) - mg);
+      const int n = min(32, np - i0);
+#pragma unroll 8
+      for (int j = 0; j < n; ++j) {
+        const float wj = __shfl_sync(~0u, w, j);
+        const float* row = acc_base + ((size_t)(i0 + j) * hs + g) * D;
+        if constexpr (C == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(row));
+          acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(row));
+          acc[0] += wj * v.x; acc[1] += wj * v.y;
+        }
+      }
+    }
+    float lg = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxGroup; ++k)
+      if (k == g) lg = L[k];
+    const float inv = 1.f / lg;
+    TO* o = out + ((size_t)d.b * p.num_q_heads + hq0 + g) * D + lane * C;
+#pragma unroll
+    for (int c = 0; c < C; c += 2) store2(o + c, acc[c] * inv, acc[c + 1] * inv);
+  }
+}
+
+// 3. merge: one warp per (sequence, KV head) with more than one partition.
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, int head_dim) {
+  griddep_wait();  // every partial of the attention kernel is written
+  griddep_launch_dependents();
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= p.num_seqs * p.num_kv_heads) return;
+  UnitDesc d;
+  d.b = w / p.num_kv_heads;
+  d.h = w - d.b * p.num_kv_heads;
+  d.part_start = p.ws.part_start[d.b];
+  d.nparts = p.ws.part_start[d.b + 1] - d.part_start;
+  if (d.nparts <= 1) return;  // written by the attention kernel (or zeroed by the plan)
+  if (head_dim == 128) {
+    if (p.out_f32 || p.out_bytes == 4) merge_partials<128, float>(p, d, static_cast<float*>(p.out), lane);
+    else if (p.out_bf16) merge_partials<128, __nv_bfloat16>(p, d, static_cast<__nv_bfloat16*>(p.out), lane);
+    else merge_partials<128, __half>(p, d, static_cast<__half*>(p.out), lane);
+  } else {
+    if (p.out_f32 || p.out_bytes == 4) merge_partials<64, float>(p, d, static_cast<float*>(p.out), lane);
+    else if (p.out_bf16) merge_partials<64, __nv_bfloat16>(p, d, static_cast<__nv_bfloat16*>(p.out), lane);
+    else merge_partials<64, __half>(p, d, static_cast<__half*>(p.out), lane);
+  }
 }
 
 // ----------------------------------------------------------------------------------
@@ -239,9 +386,9 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     prefetch_tensormap(&tmv);
   }
   __syncthreads();
+  griddep_wait();  // the plan kernel's work list is complete from here on
 
   const int total_units = p.ws.header[1];
-  const int psz = p.ws.header[2];
 
   if (warp >= C::kPairs) {
     // ------------------------------ producer warp ------------------------------
@@ -261,10 +408,11 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
           mydesc[qs].valid = 0;
           mbar_arrive(smem_addr(qfull + qs));
         }
+        griddep_launch_dependents();
         break;
       }
-      if (lane == 0) next_u = atomicAdd(p.ws.header, 1);  // fetch the next unit early
-      const UnitDesc d = describe_unit(p, u, psz);
+      if (lane == 0) next_u = atomicAdd(p.ws.header, 1);  // claim the next unit early
+      const UnitDesc d = describe_unit(load_part(p, u), u, p.num_kv_heads);
       const int ntiles = (d.ntok + BS - 1) / BS;
       const int32_t* row = p.block_tables + (size_t)d.b * p.max_blocks + d.tok0 / BS;
       int ids[kMaxPartBlocks / 32];
@@ -517,23 +665,25 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
 // ----------------------------------------------------------------------------------
 // 2b. attend: fp32 on CUDA cores (one warp per unit, one token at a time)
 // ----------------------------------------------------------------------------------
-constexpr int kMaxGroup = 16;
 
 template <int D>
 __global__ void __launch_bounds__(128) decode_f32_kernel(const float* __restrict__ k_cache,
                                                          const float* __restrict__ v_cache,
                                                          const DecodeParams p, int block_size) {
   constexpr int V = D / 32;  // elements per lane
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int total_units = p.ws.header[1];
-  const int psz = p.ws.header[2];
   for (;;) {
     int u = 0;
     if (lane == 0) u = atomicAdd(p.ws.header, 1);
     u = __shfl_sync(~0u, u, 0);
-    if (u >= total_units) return;
-    const UnitDesc d = describe_unit(p, u, psz);
+    if (u >= total_units) {
+      griddep_launch_dependents();
+      return;
+    }
+    const UnitDesc d = describe_unit(load_part(p, u), u, p.num_kv_heads);
     const float* qb = static_cast<const float*>(p.q) + ((size_t)d.b * p.num_q_heads + (size_t)d.h * G) * D;
     float qv[kMaxGroup][V], acc[kMaxGroup][V], m[kMaxGroup], l[kMaxGroup];
 #pragma unroll
@@ -598,76 +748,6 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const float* __restrict
 }
 
 // ----------------------------------------------------------------------------------
-// 3. merge partitions: out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
-// ----------------------------------------------------------------------------------
-constexpr int kMergeThreads = 128;
-constexpr int kMergeChunk = 1024;
-
-template <typename TO>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeWorkspace ws, TO* out,
-                                                                     int num_q_heads,
-                                                                     int num_kv_heads, int D) {
-  __shared__ float s_w[kMergeChunk];
-  __shared__ float s_red[kMergeThreads / 32];
-  __shared__ float s_acc[kMergeThreads];
-  const int b = blockIdx.y, h = blockIdx.x;
-  const int G = num_q_heads / num_kv_heads;
-  const int ps = ws.part_start[b];
-  const int np = ws.part_start[b + 1] - ps;
-  if (np == 1) return;  // written directly by the attention kernel
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int slices = kMergeThreads / D;  // 1 or 2
-  const int slice = tid / D, d = tid - slice * D;
-  for (int g = 0; g < G; ++g) {
-    const int hq = h * G + g;
-    TO* o = out + ((size_t)b * num_q_heads + hq) * D;
-    if (np == 0) {
-      for (int i = tid; i < D; i += kMergeThreads) store1(o + i, 0.f);
-      continue;
-    }
-    float mx = kNegInf;
-    for (int i = tid; i < np; i += kMergeThreads)
-      mx = fmaxf(mx, ws.part_ml[(size_t)(ps + i) * num_q_heads + hq].x);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
-    __syncthreads();
-    if (lane == 0) s_red[wid] = mx;
-    __syncthreads();
-    mx = s_red[0];
-    for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, s_red[w]);
-
-    float acc = 0.f, lsum = 0.f;
-    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
-      const int n = min(kMergeChunk, np - c0);
-      __syncthreads();
-      for (int i = tid; i < n; i += kMergeThreads) {
-        const float2 ml = ws.part_ml[(size_t)(ps + c0 + i) * num_q_heads + hq];
-        const float w = fast_exp2(ml.x - mx);
-        s_w[i] = w;
-        lsum += w * ml.y;
-      }
-      __syncthreads();
-      if (slice < slices)
-        for (int i = slice; i < n; i += slices)
-          acc += s_w[i] * ws.part_acc[((size_t)(ps + c0 + i) * num_q_heads + hq) * D + d];
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(~0u, lsum, off);
-    __syncthreads();
-    if (lane == 0) s_red[wid] = lsum;
-    s_acc[tid] = acc;
-    __syncthreads();
-    float L = 0.f;
-    for (int w = 0; w < kMergeThreads / 32; ++w) L += s_red[w];
-    if (slice == 0) {
-      float a = s_acc[tid];
-      for (int sl = 1; sl < slices; ++sl) a += s_acc[tid + sl * D];
-      store1(o + d, a / L);
-    }
-  }
-}
-
-// ----------------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------------
 constexpr int kMaxDev = 64;
@@ -722,7 +802,9 @@ int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) 
   const int occ = configure(slot, dev, C::kThreads, slot.smem_max);
   if (occ < 0) return fail(PA_ERR_CUDA, "pa_decode: kernel configuration failed");
   const int grid = sm_count() * occ;
-  decode_mma_kernel<T, D, BS><<<grid, C::kThreads, C::smem_bytes(p.group), stream>>>(tmk, tmv, p);
+  const cudaError_t e = launch_pdl(decode_mma_kernel<T, D, BS>, dim3(grid), dim3(C::kThreads),
+                                   C::smem_bytes(p.group), stream, tmk, tmv, p);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
   return PA_OK;
 }
 
@@ -756,7 +838,7 @@ WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head
   l.header = 0;
   l.part_start = 256;
   l.units = align_up(l.part_start + sizeof(int) * (num_seqs + 1), 256);
-  l.part_ml = align_up(l.units + sizeof(int2) * parts, 256);
+  l.part_ml = align_up(l.units + sizeof(PartRec) * parts, 256);
   l.part_acc = align_up(l.part_ml + sizeof(float2) * parts * num_q_heads, 256);
   l.total = align_up(l.part_acc + sizeof(float) * parts * num_q_heads * head_dim, 256);
   return l;
@@ -776,7 +858,7 @@ DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads, 
   DecodeWorkspace w;
   w.header = reinterpret_cast<int*>(b + l.header);
   w.part_start = reinterpret_cast<int*>(b + l.part_start);
-  w.units = reinterpret_cast<int2*>(b + l.units);
+  w.parts = reinterpret_cast<PartRec*>(b + l.units);
   w.part_ml = reinterpret_cast<float2*>(b + l.part_ml);
   w.part_acc = reinterpret_cast<float*>(b + l.part_acc);
   return w;
@@ -786,9 +868,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "pa_decode: more than 65535 sequences");
   const long long cap = std::min<long long>(a.max_ctx, (long long)a.max_blocks * a.block_size);
   const int ctx_cap = (int)std::min<long long>(cap, 0x7fffffffll);
+  const int out_row_vec16 =
+      (int)((size_t)a.num_q_heads * a.head_dim * dtype_bytes(a.out_dtype) / 16);
 
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, ctx_cap, a.num_kv_heads,
-                                             a.block_size, a.ws, a.status);
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, a.context_lens,
+                             a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
+                             static_cast<int4*>(a.out), out_row_vec16);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
   DecodeParams p;
   p.q = a.q;
   p.out = a.out;
@@ -804,38 +890,28 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
   p.out_f32 = a.out_dtype == PA_F32 && a.dtype != PA_F32;
+  p.out_bytes = (int)dtype_bytes(a.out_dtype);
+  p.out_bf16 = a.out_dtype == PA_BF16;
   p.scale_log2 = a.scale * kLog2e;
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {
-    const int grid = std::max(1, sm_count()) * 8;
-    if (a.head_dim == 128)
-      decode_f32_kernel<128><<<grid, 128, 0, stream>>>(static_cast<const float*>(a.k_cache),
-                                                       static_cast<const float*>(a.v_cache), p,
-                                                       a.block_size);
-    else
-      decode_f32_kernel<64><<<grid, 128, 0, stream>>>(static_cast<const float*>(a.k_cache),
-                                                      static_cast<const float*>(a.v_cache), p,
-                                                      a.block_size);
+    const dim3 grid(std::max(1, sm_count()) * 8);
+    const float* kc = static_cast<const float*>(a.k_cache);
+    const float* vc = static_cast<const float*>(a.v_cache);
+    e = a.head_dim == 128
+            ? launch_pdl(decode_f32_kernel<128>, grid, dim3(128), 0, stream, kc, vc, p, a.block_size)
+            : launch_pdl(decode_f32_kernel<64>, grid, dim3(128), 0, stream, kc, vc, p, a.block_size);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
   } else if (a.dtype == PA_BF16) {
     rc = launch_mma_dispatch<__nv_bfloat16>(a, p, stream);
   } else {
     rc = launch_mma_dispatch<__half>(a, p, stream);
   }
   if (rc != PA_OK) return rc;
-
-  dim3 grid(a.num_kv_heads, a.num_seqs);
-  if (a.out_dtype == PA_F32)
-    decode_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(
-        a.ws, static_cast<float*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
-  else if (a.out_dtype == PA_BF16)
-    decode_merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(
-        a.ws, static_cast<__nv_bfloat16*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
-  else
-    decode_merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(
-        a.ws, static_cast<__half*>(a.out), a.num_q_heads, a.num_kv_heads, a.head_dim);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
+  const int warps = a.num_seqs * a.num_kv_heads;
+  e = launch_pdl(decode_merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, stream, p, a.head_dim);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (merge): %s", cudaGetErrorString(e));
   return PA_OK;
 }
 

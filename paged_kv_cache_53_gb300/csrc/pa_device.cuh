@@ -226,6 +226,17 @@ __device__ __forceinline__ void store1<__half>(__half* p, float a) {
   *p = __float2half_rn(a);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so that it
+// may start while the previous kernel on the stream is still running; it must call
+// griddep_wait() before it touches memory that earlier work on the stream writes (and
+// every kernel calls it, so that completion stays transitive along the stream).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

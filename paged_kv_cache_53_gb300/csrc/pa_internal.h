@@ -60,15 +60,29 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
 // Split-KV work planning.  A sequence's context is cut into partitions of
 // `part_tokens` tokens (a multiple of the block size, chosen on the device from the
 // batch's total context so that about kTargetUnits (partition, KV head) units exist);
-// partial results of multi-partition sequences are merged by a second kernel.
-constexpr int kTargetUnits = 4096;
+// the partial results of a multi-partition sequence are merged by a third kernel.
+#ifndef PA_DECODE_TARGET_UNITS
+#define PA_DECODE_TARGET_UNITS 2048
+#endif
+constexpr int kTargetUnits = PA_DECODE_TARGET_UNITS;
 constexpr int kMinPartBlocks = 2;
 constexpr int kMaxPartBlocks = 128;
+
+// One split-KV partition of one sequence, as the plan kernel describes it.
+struct PartRec {
+  int b;           // sequence
+  int p;           // partition index within the sequence
+  int tok0;        // first context position of the partition
+  int ntok;        // positions in the partition (1 .. part_tokens)
+  int part_start;  // global index of the sequence's first partition
+  int nparts;      // partitions of the sequence
+  int pad0, pad1;
+};
 
 struct DecodeWorkspace {
   int* header;        // [0] unit counter, [1] units, [2] part_tokens, [3] partitions
   int* part_start;    // [num_seqs + 1] first partition index of each sequence
-  int2* units;        // [max_parts] (seq, partition), largest first
+  PartRec* parts;     // [max_parts] partitions, largest first
   float2* part_ml;    // [max_parts * num_q_heads] (running max in log2 units, sum)
   float* part_acc;    // [max_parts * num_q_heads * head_dim] unnormalised outputs
 };
@@ -97,7 +111,7 @@ struct DecodeArgs {
   int32_t* status;
 };
 
-// Launches plan + attention + merge kernels.  Returns PA_OK or a PA_ERR_* code (after
+// Launches the plan, attention and merge kernels.  Returns PA_OK or a PA_ERR_* code (after
 // recording the reason).
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
