@@ -60,13 +60,25 @@ def decode_algorithmic_bytes(step: W.Step, out_bytes: int) -> int:
     return kv_bytes(step) + q + o + 4 * blocks + 4 * b.num_seqs
 
 
-def measured_peaks():
+def prefill_useful_flops(step: W.Step) -> int:
+    """Causal attention flops of one prefill call: q.k and p.v over every visible
+    position of every query token, for every query head (4 * D per pair)."""
+    sh, b = step.shape, step.prefill
+    q = b.query_lens.astype(np.int64)
+    ctx0 = b.context_lens.astype(np.int64) - q
+    visible = int((q * ctx0 + q * (q + 1) // 2).sum())
+    return 4 * sh.head_dim * sh.num_q_heads * visible
+
+
+def measured_peaks(kind: str = "hbm"):
+    """HBM GB/s, or bf16 dense TFLOP/s (burst), from the driver's measurements."""
+    key, fallback = ("hbm_gbs", FALLBACK_HBM_GBS) if kind == "hbm" else ("bf16_tflops", 1900.0)
     try:
         with open(PEAKS_FILE) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -171,12 +183,13 @@ def run_ours(args, rank, world, local_rank):
             "slots": torch.empty(b.num_new_tokens, dtype=torch.int64, device=dev),
         }
     pairs = torch.from_numpy(step.cow_pairs).to(dev) if step.cow_pairs is not None else None
-    d = step.decode
-    out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
-    ws_dec = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads, sh.num_kv_heads,
-                                                   sh.head_dim, d.max_ctx, sh.block_size),
-                         dtype=torch.uint8, device=dev)
-    p = step.prefill
+    d, p = step.decode, step.prefill
+    if d is not None:
+        out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
+        ws_dec = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads,
+                                                       sh.num_kv_heads, sh.head_dim, d.max_ctx,
+                                                       sh.block_size),
+                             dtype=torch.uint8, device=dev)
     if p is not None:
         out_pre = torch.empty((p.num_new_tokens, sh.num_q_heads, sh.head_dim), dtype=tdt,
                               device=dev)
@@ -184,10 +197,11 @@ def run_ours(args, rank, world, local_rank):
                                             sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
                                             p.max_ctx, sh.block_size)
         ws_pre = torch.empty(max(16, nbytes), dtype=torch.uint8, device=dev)
-
+    q_in = {kind: vals[f"q_{kind}"] for kind in meta}
     launches_per_step = 0
 
-    def one_step(q_dec, ev=None):
+    def one_step(ev=None):
+        """The whole hot path over one batch; ev = (decode start/end, prefill start/end)."""
         nonlocal launches_per_step
         n = 0
         if pairs is not None:
@@ -197,17 +211,22 @@ def run_ours(args, rank, world, local_rank):
             pa.slot_mapping(m["slots"], m["bt"], m["cu"], m["ctx"], sh.block_size, step.num_blocks)
             pa.reshape_and_cache(vals[f"k_new_{kind}"], vals[f"v_new_{kind}"], kc, vc, m["slots"])
             n += 2
-        if ev is not None:
-            ev[0].record(stream)
-        pa.decode(out_dec, q_dec, kc, vc, meta["decode"]["bt"], meta["decode"]["ctx"], d.max_ctx,
-                  step.scale, ws_dec)
-        if ev is not None:
-            ev[1].record(stream)
-        n += 3  # plan, attend, merge
+        if d is not None:
+            if ev is not None:
+                ev[0].record(stream)
+            pa.decode(out_dec, q_in["decode"], kc, vc, meta["decode"]["bt"],
+                      meta["decode"]["ctx"], d.max_ctx, step.scale, ws_dec)
+            if ev is not None:
+                ev[1].record(stream)
+            n += 3  # plan, attend, merge
         if p is not None:
-            pa.prefill_chunk(out_pre, vals["q_prefill"], kc, vc, meta["prefill"]["bt"],
+            if ev is not None:
+                ev[2].record(stream)
+            pa.prefill_chunk(out_pre, q_in["prefill"], kc, vc, meta["prefill"]["bt"],
                              meta["prefill"]["cu"], meta["prefill"]["ctx"], p.max_q, p.max_ctx,
                              step.scale, ws_pre)
+            if ev is not None:
+                ev[3].record(stream)
             n += 1
         launches_per_step = n
 
@@ -219,115 +238,130 @@ def run_ours(args, rank, world, local_rank):
 
     # warm-up
     for _ in range(args.warmup):
-        one_step(vals["q_decode"])
+        one_step()
     barrier()
     if pa.get_status() != 0:
         raise RuntimeError("library status word set during warm-up")
 
     # timed region: inputs resident in HBM
     k = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(k)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(mk(), mk(), mk(), mk()) for _ in range(k)]
+    t0, t1 = mk(), mk()
     with ClockSampler(local_rank) as clocks:
         barrier()
         t0.record(stream)
         for i in range(k):
-            one_step(vals["q_decode"], evs[i])
+            one_step(evs[i])
         t1.record(stream)
         barrier()
     total_ms = t0.elapsed_time(t1)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    dec_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if d is not None else 0.0
+    pre_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs])) if p is not None else 0.0
     if pa.get_status() != 0:
         raise RuntimeError("library status word set during the timed region")
 
-    # end to end: the step's inputs from pinned host memory, the output back to the host
-    h_q = vals["q_decode"].cpu().pin_memory()
-    h_new = {key: vals[key].cpu().pin_memory() for key in vals if key.startswith(("k_new", "v_new"))}
-    if p is not None:
-        h_qp = vals["q_prefill"].cpu().pin_memory()
+    # end to end: the step's inputs from pinned host memory, the outputs back to the host
+    h_in = {key: vals[key].cpu().pin_memory() for key in vals
+            if key.startswith(("q_", "k_new", "v_new"))}
     h_meta = {kind: {n: m[n].cpu().pin_memory() for n in ("bt", "ctx", "cu")}
               for kind, m in meta.items()}
-    h_out = torch.empty(out_dec.shape, dtype=tdt).pin_memory()
-    d_q = torch.empty_like(vals["q_decode"])
-    h2d = h_q.numel() * h_q.element_size() + sum(t.numel() * t.element_size() for t in h_new.values())
+    outs = ([out_dec] if d is not None else []) + ([out_pre] if p is not None else [])
+    h_outs = [torch.empty(o.shape, dtype=tdt).pin_memory() for o in outs]
+    d_in = {key: torch.empty_like(vals[key]) for key in h_in}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     h2d += sum(t.numel() * t.element_size() for m in h_meta.values() for t in m.values())
-    if p is not None:
-        h2d += h_qp.numel() * h_qp.element_size()
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in h_outs)
     ke = max(1, min(k, args.e2e_steps))
+    saved = dict(vals), dict(q_in)
+    for key, t in d_in.items():  # the e2e steps read their inputs from the copies
+        if key.startswith("q_"):
+            q_in[key[2:]] = t
+        else:
+            vals[key] = t
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = mk(), mk()
     e0.record(stream)
     for _ in range(ke):
-        d_q.copy_(h_q, non_blocking=True)
-        for key, t in h_new.items():
-            vals[key].copy_(t, non_blocking=True)
+        for key, t in h_in.items():
+            d_in[key].copy_(t, non_blocking=True)
         for kind, m in h_meta.items():
             for n, t in m.items():
                 meta[kind][n].copy_(t, non_blocking=True)
-        if p is not None:
-            vals["q_prefill"].copy_(h_qp, non_blocking=True)
-        one_step(d_q)
-        h_out.copy_(out_dec, non_blocking=True)
+        one_step()
+        for ho, o in zip(h_outs, outs):
+            ho.copy_(o, non_blocking=True)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / ke
+    vals.update(saved[0])
+    q_in.update(saved[1])
 
     step_ms = total_ms / k
-    times = np.array([step_ms, dec_ms, e2e_ms], dtype=np.float64)
+    times = np.array([step_ms, dec_ms, pre_ms, e2e_ms], dtype=np.float64)
     if world > 1:
-        import torch
         import torch.distributed as dist
         t = torch.tensor(times, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         times = t.cpu().numpy()
-    step_ms, dec_ms, e2e_ms = [float(x) for x in times]
+    step_ms, dec_ms, pre_ms, e2e_ms = [float(x) for x in times]
 
-    kvb = kv_bytes(step)
-    kv_tokens = int(d.context_lens.astype(np.int64).sum())
-    value = world * kvb / (step_ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-    alg = decode_algorithmic_bytes(step, out_dec.element_size())
-    achieved = alg / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
-    res = {
-        "metric": METRIC,
-        "value": round(value, 1),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": k,
-        "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": sh.dtype,
-        "data": "synthetic",
-        "config": {
-            "workload": step.name,
-            "num_seqs": d.num_seqs, "num_q_heads": sh.num_q_heads,
-            "num_kv_heads": sh.num_kv_heads, "head_dim": sh.head_dim,
-            "block_size": sh.block_size, "kv_tokens_per_step": kv_tokens,
-            "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
-            "prefill_tokens": p.num_new_tokens if p is not None else 0,
-            "cow_copies": int(step.cow_pairs.shape[0]) if step.cow_pairs is not None else 0,
-            "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV read per step vs 0.13 GB L2",
-            "parallelism": f"replicas x{world}",
-        },
-        "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),
-        "hbm_frac_of_measured": round(value / peak, 4),
-        "clocks": clocks.summary(),
-        "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_ms, 5), "steps": ke},
-        "gpu_launches": launches_per_step * k,
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (plan + attend + merge)",
-                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": alg,
-                     "ms_per_launch": round(dec_ms, 5)},
+    config = {
+        "workload": step.name, "num_q_heads": sh.num_q_heads, "num_kv_heads": sh.num_kv_heads,
+        "head_dim": sh.head_dim, "block_size": sh.block_size,
+        "cow_copies": int(step.cow_pairs.shape[0]) if step.cow_pairs is not None else 0,
+        "parallelism": f"replicas x{world}",
     }
+    res = {"metric": METRIC, "n_gpus": world, "steps": k, "warmup": args.warmup,
+           "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": sh.dtype, "data": "synthetic", "config": config}
+    if p is not None:
+        flops = prefill_useful_flops(step)
+        tpeak, tkind = measured_peaks("tensor")
+        pre = {"ms_per_call": round(pre_ms, 5), "useful_gflop": round(flops / 1e9, 2),
+               "achieved": round(flops / (pre_ms * 1e-3) / 1e12, 1), "peak": tpeak,
+               "peak_kind": tkind, "unit": "TFLOP/s",
+               "frac": round(flops / (pre_ms * 1e-3) / 1e12 / tpeak, 4),
+               "tokens": p.num_new_tokens, "max_ctx": p.max_ctx}
+        config["prefill_tokens"] = p.num_new_tokens
+    if d is not None:
+        kvb = kv_bytes(step)
+        kv_tokens = int(d.context_lens.astype(np.int64).sum())
+        peak, peak_kind = measured_peaks()
+        alg = decode_algorithmic_bytes(step, out_dec.element_size())
+        achieved = alg / (dec_ms * 1e-3) / 1e9
+        config.update({"num_seqs": d.num_seqs, "kv_tokens_per_step": kv_tokens,
+                       "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
+                       "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV read per step "
+                             "vs 0.13 GB L2"})
+        res.update({
+            "value": round(world * kvb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),
+            "hbm_frac_of_measured": round(kvb / (step_ms * 1e-3) / 1e9 / peak, 4),
+            "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 5), "steps": ke},
+            "roofline": {"bound": "hbm", "kernel": "pa_decode (plan + attend + merge)",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic(args.workload), "algorithmic_bytes": alg,
+                         "ms_per_launch": round(dec_ms, 5)},
+        })
+        if p is not None:
+            res["prefill"] = pre
+    else:  # a prefill-only workload: useful causal TFLOP/s against the tensor roofline
+        flops = prefill_useful_flops(step)
+        res.update({
+            "metric": "chunked-prefill attention useful TFLOP/s",
+            "value": round(world * flops / (step_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 5), "steps": ke},
+            "roofline": dict(pre, bound="tensor", kernel="pa_prefill_chunk",
+                             traffic=recorded_traffic(args.workload)),
+        })
+    res["clocks"] = clocks.summary()
+    res["gpu_launches"] = launches_per_step * k
     return res, step
 
 
@@ -510,7 +544,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res, step = run_ours(args, rank, world, local_rank)
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and step.decode is not None:
         res["cpu_baseline"] = cpu_baseline(step, args.cpu_budget_s)
     if world > 1:
         import torch.distributed as dist

@@ -318,12 +318,22 @@ def mixed_prefill_decode(decode_scale: float = 1.0) -> Step:
         prefill=Batch(pre_ctx, np.full(8, chunk, dtype=np.int32), pre_tables))
 
 
+def mixed_prefill_only() -> Step:
+    """The mixed workload's prefill batch alone (8 chunks of 512 over the same contexts),
+    on a pool that holds just its blocks: the chunked-prefill case for timing and
+    profiling."""
+    pre = mixed_prefill_decode().prefill
+    return prefill_step("mixed_prefill8x512_h32kv8_d128_bf16_bs32", Shape(32, 8, 128, 32, "bf16"),
+                        pre.context_lens, pre.query_lens, 53_004)
+
+
 NAMED = {
     "tiny_decode": tiny_decode,
     "opt13b_decode": opt13b_decode,
     "llama8b_gqa_decode": llama8b_gqa_decode,
     "prefix_sharing_cow": prefix_sharing_cow,
     "mixed_prefill_decode": mixed_prefill_decode,
+    "mixed_prefill_only": mixed_prefill_only,
 }
 
 
