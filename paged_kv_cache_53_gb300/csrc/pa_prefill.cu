@@ -38,8 +38,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
+struct PrefillItem;
+
 struct PrefillParams {
   void* out;
+  const PrefillItem* items;
+  const int* header;
   const int32_t* block_tables;
   const int32_t* cu_q_lens;
   const int32_t* context_lens;
@@ -50,7 +54,8 @@ struct PrefillParams {
 
 template <int D, int BS>
 struct PrefillCfg {
-  static constexpr int BM = 128;                       // query rows per CTA
+  static constexpr int BM = 128;                       // query rows per tile
+  static constexpr int kTiles = 2;                     // query tiles per CTA (ping-pong)
   static constexpr int BN = 64;                        // context tokens per K/V tile
   static constexpr int kHalves = D / 64;               // 128-byte column groups
   static constexpr int kQHalfBytes = BM * 128;         // 16 KiB
@@ -58,17 +63,17 @@ struct PrefillCfg {
   static constexpr int kKvHalfBytes = BN * 128;        // 8 KiB
   static constexpr int kKBytes = kHalves * kKvHalfBytes;
   static constexpr int kStageBytes = 2 * kKBytes;      // K then V
-  static constexpr int kStages = 3;
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kPBytes = BM * BN * 2;          // one 16-bit P term, 16 KiB
   static constexpr int kPBufBytes = 2 * kPBytes;       // hi + lo
   static constexpr int kBlocksPerTile = BN / BS;
-  static constexpr int kThreads = 256;
-  static constexpr int kTmemCols = 256;                // S0 | S1 | O
-  // barriers: q_full, kv_full[3], kv_empty[3], s_full[2], s_free[2], p_full[2],
-  // p_empty[2], o_full
-  static constexpr int kBars = 16;
-  static constexpr size_t kSmem =
-      1024 + kQBytes + (size_t)kStages * kStageBytes + 2 * kPBufBytes + kBars * 8 + 16;
+  static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 x softmax WG
+  static constexpr int kTmemCols = 512;                // S_A | S_B | O_A | O_B
+  // barriers: q_full, kv_full[S], kv_empty[S], then per query tile s_full, s_free,
+  // p_full, p_empty, o_full
+  static constexpr int kBars = 1 + 2 * kStages + 5 * kTiles;
+  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
+                                  kTiles * (size_t)kPBufBytes + kBars * 8 + 16;
 };
 
 template <typename T>
@@ -98,50 +103,154 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// ----------------------------------------------------------------------------------
+// plan: one work item per (sequence, KV head, pair of query tiles), heaviest first
+// ----------------------------------------------------------------------------------
+struct PrefillItem {
+  int b, h, ctile, pad;
+};
+
+constexpr int kPlanBuckets = 4096;
+constexpr int kPlanThreads = 1024;
+
+// Items are bucketed by how many K/V tiles their later query tile needs (>> key_shift)
+// and written in decreasing order, so that CTA i, which takes item i, starts the long
+// causal rows first and the grid ends on the short ones.
+__global__ void __launch_bounds__(kPlanThreads)
+    prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens,
+                        const int32_t* __restrict__ context_lens, int num_seqs,
+                        int num_kv_heads, int group, int rows_per_item, int bn, int key_shift,
+                        long long max_ctx, PrefillItem* __restrict__ items,
+                        int* __restrict__ header, int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int s_hist[kPlanBuckets];
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < kPlanBuckets; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  const int tpt = rows_per_item / group;  // chunk tokens per item
+  auto bucket = [&](int ctx0, int chunk, int ct) {
+    const int t_last = min(chunk, (ct + 1) * tpt) - 1;
+    const int n_kv = (ctx0 + t_last) / bn + 1;
+    return kPlanBuckets - 1 - min(kPlanBuckets - 1, n_kv >> key_shift);  // heaviest first
+  };
+  for (int b = tid; b < num_seqs; b += blockDim.x) {
+    const int chunk = cu_q_lens[b + 1] - cu_q_lens[b];
+    const int ctx0 = context_lens[b] - chunk;
+    if (chunk <= 0) continue;
+    if (ctx0 < 0 || context_lens[b] > max_ctx) {  // such a sequence gets no output rows
+      flag_status(status, PA_STATUS_BAD_CONTEXT);
+      continue;
+    }
+    const int ncts = (chunk + tpt - 1) / tpt;
+    for (int ct = 0; ct < ncts; ++ct) atomicAdd(&s_hist[bucket(ctx0, chunk, ct)], num_kv_heads);
+  }
+  __syncthreads();
+  // exclusive scan of the histogram: each thread owns kPlanBuckets / blockDim buckets
+  constexpr int per = kPlanBuckets / kPlanThreads;
+  int v[per], run = 0;
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    v[k] = s_hist[tid * per + k];
+    run += v[k];
+  }
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = s_warp[lane];
+    int iw = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(~0u, iw, o);
+      if (lane >= o) iw += t;
+    }
+    s_warp[lane] = iw - w;
+    if (lane == 31) header[0] = iw;
+  }
+  __syncthreads();
+  int off = s_warp[wid] + incl - run;
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    s_hist[tid * per + k] = off;
+    off += v[k];
+  }
+  __syncthreads();
+  for (int b = tid; b < num_seqs; b += blockDim.x) {
+    const int chunk = cu_q_lens[b + 1] - cu_q_lens[b];
+    const int ctx0 = context_lens[b] - chunk;
+    if (chunk <= 0 || ctx0 < 0 || context_lens[b] > max_ctx) continue;
+    const int ncts = (chunk + tpt - 1) / tpt;
+    for (int ct = 0; ct < ncts; ++ct) {
+      const int slot = atomicAdd(&s_hist[bucket(ctx0, chunk, ct)], num_kv_heads);
+      for (int h = 0; h < num_kv_heads; ++h) items[slot + h] = PrefillItem{b, h, ct, 0};
+    }
+  }
+}
+
+// Per query tile of a CTA: where it starts in the chunk and how far it reaches.
+struct TileGeom {
+  int t0;       // first chunk token
+  int ntok;     // chunk tokens in the tile (0: the tile lies past the chunk)
+  int n_kv;     // K/V tiles it needs (0 if ntok == 0)
+};
+
 template <typename T, int D, int BS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   using C = PrefillCfg<D, BS>;
-  constexpr int BN = C::BN, S = C::kStages;
+  constexpr int BN = C::BN, S = C::kStages, NT = C::kTiles;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sKV = sQ + C::kQBytes;
-  uint8_t* sP = sKV + S * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::kPBufBytes);
+  uint8_t* sQ = base;                              // [tile][half][128 rows][128 B]
+  uint8_t* sKV = sQ + NT * C::kQBytes;             // [stage][K | V][half][64 rows][128 B]
+  uint8_t* sP = sKV + S * C::kStageBytes;          // [tile][hi | lo][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + NT * C::kPBufBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + S;
-  uint64_t* s_full = bars + 1 + 2 * S;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* p_empty = p_full + 2;
-  uint64_t* o_full = p_empty + 2;
+  uint64_t* s_full = bars + 1 + 2 * S;  // [tile]
+  uint64_t* s_free = s_full + NT;
+  uint64_t* p_full = s_free + NT;
+  uint64_t* p_empty = p_full + NT;
+  uint64_t* o_full = p_empty + NT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = p.group;
-  const int tpt = C::BM / G;  // chunk tokens per tile
+  const int tpt = C::BM / G;  // chunk tokens per query tile
 
-  griddep_wait();  // the chunk's K/V were written by the preceding cache write
+  griddep_wait();  // the work list and the chunk's K/V (cache write) are complete
+  if ((int)blockIdx.x >= __ldg(p.header)) return;  // more CTAs launched than items
+  const PrefillItem item = p.items[blockIdx.x];
+  const int h = item.h, b = item.b;
   const int q_begin = __ldg(p.cu_q_lens + b);
   const int chunk = __ldg(p.cu_q_lens + b + 1) - q_begin;
-  const int t0 = qtile * tpt;
-  if (t0 >= chunk) return;  // the whole CTA leaves before touching any barrier
+  const int t0_cta = item.ctile * NT * tpt;
+  if (t0_cta >= chunk) return;  // the whole CTA leaves before touching any barrier
   const int ctx = __ldg(p.context_lens + b);
   if (ctx < chunk || (long long)ctx > (long long)p.max_blocks * BS) {
-    if (threadIdx.x == 0 && qtile == 0) flag_status(p.status, PA_STATUS_BAD_CONTEXT);
+    if (threadIdx.x == 0 && item.ctile == 0 && h == 0) flag_status(p.status, PA_STATUS_BAD_CONTEXT);
     return;
   }
   const int ctx0 = ctx - chunk;
-  const int ntok = min(tpt, chunk - t0);    // chunk tokens of this tile
-  const int rows_valid = ntok * G;
-  const int last_pos = ctx0 + t0 + ntok - 1;  // position of the tile's last query
-  const int n_kv = last_pos / BN + 1;         // K/V tiles it needs
   const int nblk_ctx = (ctx + BS - 1) / BS;
+  TileGeom tg[NT];
+#pragma unroll
+  for (int x = 0; x < NT; ++x) {
+    tg[x].t0 = t0_cta + x * tpt;
+    tg[x].ntok = max(0, min(tpt, chunk - tg[x].t0));
+    tg[x].n_kv = tg[x].ntok > 0 ? (ctx0 + tg[x].t0 + tg[x].ntok - 1) / BN + 1 : 0;
+  }
+  const int n_kv = tg[NT - 1].ntok > 0 ? tg[NT - 1].n_kv : tg[0].n_kv;  // the CTA's K/V tiles
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(q_full), 1);
@@ -149,13 +258,13 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(smem_addr(kv_full + i), 1);
       mbar_init(smem_addr(kv_empty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(s_full + i), 1);
-      mbar_init(smem_addr(s_free + i), 128);
-      mbar_init(smem_addr(p_full + i), 128);
-      mbar_init(smem_addr(p_empty + i), 1);
+    for (int x = 0; x < NT; ++x) {
+      mbar_init(smem_addr(s_full + x), 1);
+      mbar_init(smem_addr(s_free + x), 128);
+      mbar_init(smem_addr(p_full + x), 128);
+      mbar_init(smem_addr(p_empty + x), 1);
+      mbar_init(smem_addr(o_full + x), 1);
     }
-    mbar_init(smem_addr(o_full), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -171,17 +280,25 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // TMEM columns: S of tile x at x * BN, O of tile x at NT * BN + x * D
   bool ok = true;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other tiles
+    const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other CTAs
     if (lane == 0) {
-      mbar_arrive_expect_tx(smem_addr(q_full), C::kQBytes);
+      int qbytes = 0;
 #pragma unroll
-      for (int hb = 0; hb < C::kHalves; ++hb)
-        tma_load_3d(smem_addr(sQ + hb * C::kQHalfBytes), &tmq, hb * 64, h * G, q_begin + t0,
-                    smem_addr(q_full), keep);
+      for (int x = 0; x < NT; ++x) qbytes += tg[x].ntok > 0 ? C::kQBytes : 0;
+      mbar_arrive_expect_tx(smem_addr(q_full), qbytes);
+#pragma unroll
+      for (int x = 0; x < NT; ++x) {
+        if (tg[x].ntok == 0) continue;
+#pragma unroll
+        for (int hb = 0; hb < C::kHalves; ++hb)
+          tma_load_3d(smem_addr(sQ + x * C::kQBytes + hb * C::kQHalfBytes), &tmq, hb * 64, h * G,
+                      q_begin + tg[x].t0, smem_addr(q_full), keep);
+      }
     }
     const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
     for (int j = 0; j < n_kv && ok; ++j) {
@@ -217,15 +334,33 @@ __global__ void __launch_bounds__(256, 1)
     if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
+    // order: S_A(j), S_B(j), PV_A(j-1), PV_B(j-1), so that while one tile's softmax
+    // runs the tensor core works on the other tile
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM, BN, false, false);
       const uint32_t id_o = tc::idesc_f16(Fmt<T>::v, C::BM, D, false, true);
-      const uint32_t tO = tmem + 2 * BN;
-      auto issue_pv = [&](int jj) -> bool {
-        if (!mbar_wait(smem_addr(p_full + (jj & 1)), (jj >> 1) & 1)) return false;
+      auto issue_s = [&](int x, int j) -> bool {
+        if (!mbar_wait(smem_addr(s_free + x), (j - 1) & 1)) return false;
         tc::fence_after_sync();
+        const uint32_t tS = tmem + x * BN;
+        const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
+        const uint32_t sk = smem_addr(sKV + (j % S) * C::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t a = tc::smem_desc_sw128(sq + (kk >> 2) * C::kQHalfBytes + koff, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(sk + (kk >> 2) * C::kKvHalfBytes + koff, 16, 1024);
+          tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
+        }
+        tc::commit(smem_addr(s_full + x));
+        return true;
+      };
+      auto issue_pv = [&](int x, int jj) -> bool {
+        if (!mbar_wait(smem_addr(p_full + x), jj & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t tO = tmem + NT * BN + x * D;
         const uint32_t sv = smem_addr(sKV + (jj % S) * C::kStageBytes + C::kKBytes);
-        const uint32_t sp = smem_addr(sP + (jj & 1) * C::kPBufBytes);
+        const uint32_t sp = smem_addr(sP + x * C::kPBufBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
@@ -234,124 +369,117 @@ __global__ void __launch_bounds__(256, 1)
           tc::mma_f16_ss(tO, ahi, bdesc, id_o, jj > 0 || ks > 0);
           tc::mma_f16_ss(tO, alo, bdesc, id_o, true);
         }
-        tc::commit(smem_addr(p_empty + (jj & 1)));
-        tc::commit(smem_addr(kv_empty + (jj % S)));
+        tc::commit(smem_addr(p_empty + x));
+        if (jj == tg[x].n_kv - 1) tc::commit(smem_addr(o_full + x));
         return true;
       };
       if (!mbar_wait(smem_addr(q_full), 0)) ok = false;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % S;
-        if (!mbar_wait(smem_addr(kv_full + s), (j / S) & 1)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(smem_addr(s_free + (j & 1)), ((j - 2) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        const uint32_t tS = tmem + (j & 1) * BN;
-        const uint32_t sq = smem_addr(sQ), sk = smem_addr(sKV + s * C::kStageBytes);
+      for (int j = 0; j <= n_kv && ok; ++j) {
+        if (j < n_kv) {
+          if (!mbar_wait(smem_addr(kv_full + j % S), (j / S) & 1)) { ok = false; break; }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk & 3) * 32;
-          const uint64_t a = tc::smem_desc_sw128(sq + (kk >> 2) * C::kQHalfBytes + koff, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(sk + (kk >> 2) * C::kKvHalfBytes + koff, 16, 1024);
-          tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
+          for (int x = 0; x < NT; ++x)
+            if (j < tg[x].n_kv && !issue_s(x, j)) ok = false;
         }
-        tc::commit(smem_addr(s_full + (j & 1)));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (j >= 1) {
+#pragma unroll
+          for (int x = 0; x < NT; ++x)
+            if (j - 1 < tg[x].n_kv && ok && !issue_pv(x, j - 1)) ok = false;
+          tc::commit(smem_addr(kv_empty + (j - 1) % S));
+        }
       }
-      if (ok && !issue_pv(n_kv - 1)) ok = false;
-      if (ok) tc::commit(smem_addr(o_full));
       if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------ softmax / epilogue ------------------------------
-    const int r = threadIdx.x - 128;                         // row of the tile = TMEM lane
-    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int rpos = ctx0 + t0 + r / G;                      // position of this row's query
+    // --------------------------- softmax / epilogue (one WG per tile) ---------------------------
+    const int x = (warp - 4) >> 2;                           // query tile of this warpgroup
+    const int r = (threadIdx.x - 128) & 127;                 // row of the tile = TMEM lane
+    const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + x * BN;
+    const uint32_t tO = tmem + lane_bits + NT * BN + x * D;
+    const TileGeom g = x == 0 ? tg[0] : tg[NT - 1];
+    const int rpos = ctx0 + g.t0 + r / G;                    // position of this row's query
     float m = kNegInf, l = 0.f;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait(smem_addr(s_full + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+    for (int j = 0; j < g.n_kv; ++j) {
+      if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      float x[BN];
-      tc::tmem_ld32(trow + (j & 1) * BN, *reinterpret_cast<float(*)[32]>(x));
-      tc::tmem_ld32(trow + (j & 1) * BN + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      float xs[BN];
+      tc::tmem_ld32(tS, *reinterpret_cast<float(*)[32]>(xs));
+      tc::tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(xs + 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
-      mbar_arrive(smem_addr(s_free + (j & 1)));
+      mbar_arrive(smem_addr(s_free + x));
 
       const int kp0 = j * BN;
       float mx = kNegInf;
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
-        x[c] = (kp0 + c <= rpos) ? x[c] * p.scale_log2 : kNegInf;
-        mx = fmaxf(mx, x[c]);
+        xs[c] = (kp0 + c <= rpos) ? xs[c] * p.scale_log2 : kNegInf;
+        mx = fmaxf(mx, xs[c]);
       }
       const bool need = mx > m + kRescaleThreshold;
-      if (__any_sync(~0u, need)) {
-        const float alpha = need ? fast_exp2(m - mx) : 1.f;
-        if (j > 0) {
-          // O holds P_0..j-1 V: wait for the last of those products, then rescale
-          if (!mbar_wait(smem_addr(p_empty + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
-          tc::fence_after_sync();
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float o[32];
-            tc::tmem_ld32(trow + 2 * BN + c0, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::tmem_st32(trow + 2 * BN + c0, o);
-          }
-          tc::tmem_wait_st();
-        }
-        if (need) {
-          l *= alpha;
-          m = mx;
-        }
-      }
+      const float alpha = need ? fast_exp2(m - mx) : 1.f;
+      if (need) m = mx;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
-        x[c] = fast_exp2(x[c] - m);
-        sum += x[c];
+        xs[c] = fast_exp2(xs[c] - m);
+        sum += xs[c];
       }
-      l += sum;
-      if (j >= 2 && !mbar_wait(smem_addr(p_empty + (j & 1)), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      const uint32_t sp = smem_addr(sP + (j & 1) * C::kPBufBytes) + r * 128;
+      l = l * alpha + sum;
+      // the previous P.V must be complete before O is rescaled or P is overwritten
+      if (j >= 1 && !mbar_wait(smem_addr(p_empty + x), (j - 1) & 1)) { ok = false; break; }
+      if (j >= 1 && __any_sync(~0u, need)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tc::tmem_ld32(tO + c0, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tc::tmem_st32(tO + c0, o);
+        }
+        tc::tmem_wait_st();
+      }
+      const uint32_t sp = smem_addr(sP + x * C::kPBufBytes) + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < BN / 8; ++c8) {
         uint4 hi, lo;
-        pack8_split<T>(x + 8 * c8, hi, lo);
+        pack8_split<T>(xs + 8 * c8, hi, lo);
         const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
         st_shared_v4(sp + off, hi);
         st_shared_v4(sp + C::kPBytes + off, lo);
       }
-      if (j == n_kv - 1) {
-        // V rows of the last tile past the context (inside its last block) may hold
-        // anything, NaN bits included, and would meet P = 0: zero them
-        const int z0 = ctx - kp0, z1 = min(BN, nblk_ctx * BS - kp0);
-        if (z0 < z1) {
-          const int s = j % S;
-          if (!mbar_wait(smem_addr(kv_full + s), (j / S) & 1)) { ok = false; break; }
-          const uint32_t sv = smem_addr(sKV + s * C::kStageBytes + C::kKBytes);
-          for (int i = r; i < (z1 - z0) * (D / 8); i += 128) {
-            const int vr = z0 + i / (D / 8), c = i % (D / 8);
-            st_shared_v4(sv + (c >> 3) * C::kKvHalfBytes + vr * 128 + (c & 7) * 16,
-                         make_uint4(0, 0, 0, 0));
-          }
+      // V rows of the context's last K/V tile past the context (inside its last block)
+      // may hold anything, NaN bits included, and would meet P = 0: zero them.  Both
+      // warpgroups may do it; they write the same zeros.
+      const int z0 = ctx - kp0, z1 = min(BN, nblk_ctx * BS - kp0);
+      if (z0 < z1) {
+        const int s = j % S;
+        if (!mbar_wait(smem_addr(kv_full + s), (j / S) & 1)) { ok = false; break; }
+        const uint32_t sv = smem_addr(sKV + s * C::kStageBytes + C::kKBytes);
+        for (int i = r; i < (z1 - z0) * (D / 8); i += 128) {
+          const int vr = z0 + i / (D / 8), c = i % (D / 8);
+          st_shared_v4(sv + (c >> 3) * C::kKvHalfBytes + vr * 128 + (c & 7) * 16,
+                       make_uint4(0, 0, 0, 0));
         }
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      mbar_arrive(smem_addr(p_full + (j & 1)));
+      mbar_arrive(smem_addr(p_full + x));
     }
     // epilogue: O / l -> out rows
-    if (ok && mbar_wait(smem_addr(o_full), 0)) {
+    if (ok && g.n_kv > 0 && mbar_wait(smem_addr(o_full + x), 0)) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
-      const size_t orow = ((size_t)(q_begin + t0 + r / G) * p.num_q_heads + h * G + r % G) * D;
+      const int rows_valid = g.ntok * G;
+      const size_t orow = ((size_t)(q_begin + g.t0 + r / G) * p.num_q_heads + h * G + r % G) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
-        tc::tmem_ld32(trow + 2 * BN + c0, o);
+        tc::tmem_ld32(tO + c0, o);
         tc::tmem_wait_ld();
         if (r < rows_valid) {
           if (p.out_f32) {
@@ -389,6 +517,13 @@ __global__ void __launch_bounds__(256, 1)
 // ----------------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------------
+// Upper bound on the work items of a call: every sequence's chunk at its maximum.
+long long prefill_max_items(int num_seqs, int max_q, int num_q_heads, int num_kv_heads) {
+  const long long rows_per_item = 128 * 2;  // PrefillCfg<>::BM * kTiles
+  const long long per_seq = ((long long)max_q * (num_q_heads / num_kv_heads) + rows_per_item - 1) /
+                            rows_per_item;
+  return (long long)num_seqs * num_kv_heads * per_seq;
+}
 constexpr int kMaxDev = 64;
 std::mutex g_mutex;
 
@@ -433,12 +568,22 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   p.num_blocks = a.num_blocks;
   p.out_f32 = a.out_dtype == PA_F32;
   p.scale_log2 = a.scale * kLog2e;
-  const long long tiles = ((long long)a.max_q * G + C::BM - 1) / C::BM;
-  if (tiles > 0x7fffffffll || a.num_seqs > 65535 || a.num_kv_heads > 65535)
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: grid too large");
-  const cudaError_t e = launch_pdl(prefill_kernel<T, D, BS>,
-                                   dim3((unsigned)tiles, a.num_kv_heads, a.num_seqs),
-                                   dim3(C::kThreads), C::kSmem, stream, tmq, tmk, tmv, p);
+  const long long items = prefill_max_items(a.num_seqs, a.max_q, a.num_q_heads, a.num_kv_heads);
+  if (items > 0x7fffffffll) return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: grid too large");
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  p.header = reinterpret_cast<int*>(ws);
+  p.items = reinterpret_cast<const PrefillItem*>(ws + 256);
+  int key_shift = 0;
+  while (((long long)a.max_ctx / C::BN + 1) >> key_shift >= kPlanBuckets) ++key_shift;
+  cudaError_t e = launch_pdl(prefill_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream,
+                             a.cu_q_lens, a.context_lens, a.num_seqs, a.num_kv_heads, G,
+                             C::BM * C::kTiles, C::BN, key_shift,
+                             std::min<long long>(a.max_ctx, (long long)a.max_blocks * a.block_size),
+                             reinterpret_cast<PrefillItem*>(ws + 256), reinterpret_cast<int*>(ws),
+                             a.status);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_prefill_chunk (plan): %s", cudaGetErrorString(e));
+  e = launch_pdl(prefill_kernel<T, D, BS>, dim3((unsigned)items), dim3(C::kThreads), C::kSmem,
+                 stream, tmq, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_prefill_chunk: %s", cudaGetErrorString(e));
   return PA_OK;
 }
@@ -455,7 +600,11 @@ int dispatch(const PrefillArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int, int, int, int, int, int, int, int) { return 0; }
+size_t prefill_workspace_bytes(int num_seqs, int, int max_q, int num_q_heads, int num_kv_heads,
+                               int, int, int) {
+  return 256 + sizeof(PrefillItem) *
+                   (size_t)prefill_max_items(num_seqs, max_q, num_q_heads, num_kv_heads);
+}
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   return a.dtype == PA_BF16 ? dispatch<__nv_bfloat16>(a, stream) : dispatch<__half>(a, stream);
