@@ -3,24 +3,26 @@
 // A chunk of prompt tokens attends causally to its sequence's whole context, the chunk
 // included ("PagedAttention and Continuous Batching Explained (2026)", section "Chunked
 // prefill").  The work is a dense contraction: for KV head h, the (chunk token, query
-// head of h's group) pairs form the rows of Q, and each 64-token tile of context is a
+// head of h's group) pairs form the rows of Q, and each 128-token tile of context is a
 // K/V block of the product.
 //
-// One CTA owns 128 query rows of one (sequence, KV head); row r is token r / G of its
-// slice of the chunk and query head h * G + r % G, so a tile covers 128 / G consecutive
-// chunk tokens and every row of it shares the same K/V.  Warp roles:
-//   warp 0     TMA producer: the Q tile once (a 3-D box over [token, head, dim]), then
-//              every K/V tile (one 2-D box per block and 64-column half, gathered
-//              through the block table, 128-byte swizzle) into a 3-stage ring.
-//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers, then
-//              O += P_j V_j into a TMEM accumulator, with P_j carried as the sum of a
-//              bf16/fp16 "hi" term and the rounding residual "lo" (two MMAs), since a
-//              single 16-bit P alone can miss a 2e-3 absolute tolerance on short
-//              contexts.  tcgen05.commit signals the barriers.
-//   warps 4-7  softmax, one thread per row: read S_j from TMEM, apply scale and the
-//              causal mask, keep the running max (moved only when it grows by more than
-//              2^8, rescaling O in TMEM then) and sum, write P_j to swizzled shared
-//              memory; at the end normalise O and store the rows.
+// A plan kernel lists one work item per (sequence, KV head, pair of 128-row query
+// tiles), heaviest first; CTA i takes item i.  Row r of a query tile is token r / G of
+// its slice of the chunk and query head h * G + r % G, so a tile covers 128 / G
+// consecutive chunk tokens and every row of it shares the same K/V.  Warp roles:
+//   warp 0     TMA producer: both Q tiles once (3-D boxes over [token, head, dim]),
+//              then every K/V tile (one 2-D box per block and 64-column half, gathered
+//              through the block table, 128-byte swizzle) into a ring of stages.
+//   warp 1     MMA issuer (one thread): S_x(j) = Q_x K_j^T into TMEM, then
+//              O_x += P_x(j) V_j with P read from TMEM, in the order PV_A(j), S_A(j+1),
+//              PV_B(j), S_B(j+1), so that one tile's softmax overlaps the other tile's
+//              products.  P is carried as the sum of a bf16/fp16 "hi" term and its
+//              rounding residual "lo" (two MMAs): a single 16-bit P alone can miss a 2e-3
+//              absolute tolerance on short contexts.
+//   warps 4-11 two softmax warpgroups, one per query tile, one thread per row: read
+//              S from TMEM, apply scale and the causal mask, keep the running max
+//              (moved only when it grows by more than 2^8, rescaling O in TMEM then) and
+//              sum, write P over S's own TMEM columns; at the end normalise O and store.
 // Tiles wholly above the diagonal are never loaded; only the last K/V tile can hold
 // positions past the context, whose V rows are zeroed before they meet P = 0.
 #include <algorithm>
@@ -56,24 +58,21 @@ template <int D, int BS>
 struct PrefillCfg {
   static constexpr int BM = 128;                       // query rows per tile
   static constexpr int kTiles = 2;                     // query tiles per CTA (ping-pong)
-  static constexpr int BN = 64;                        // context tokens per K/V tile
+  static constexpr int BN = 128;                       // context tokens per K/V tile
   static constexpr int kHalves = D / 64;               // 128-byte column groups
   static constexpr int kQHalfBytes = BM * 128;         // 16 KiB
   static constexpr int kQBytes = kHalves * kQHalfBytes;
-  static constexpr int kKvHalfBytes = BN * 128;        // 8 KiB
+  static constexpr int kKvHalfBytes = BN * 128;        // 16 KiB
   static constexpr int kKBytes = kHalves * kKvHalfBytes;
   static constexpr int kStageBytes = 2 * kKBytes;      // K then V
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kPBytes = BM * BN * 2;          // one 16-bit P term, 16 KiB
-  static constexpr int kPBufBytes = 2 * kPBytes;       // hi + lo
+  static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kBlocksPerTile = BN / BS;
   static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 x softmax WG
-  static constexpr int kTmemCols = 512;                // S_A | S_B | O_A | O_B
-  // barriers: q_full, kv_full[S], kv_empty[S], then per query tile s_full, s_free,
-  // p_full, p_empty, o_full
-  static constexpr int kBars = 1 + 2 * kStages + 5 * kTiles;
+  static constexpr int kTmemCols = 512;                // S/P_A | S/P_B | O_A | O_B
+  // barriers: q_full, kv_full[S], kv_empty[S], then per query tile s_full, p_full, pv_done
+  static constexpr int kBars = 1 + 2 * kStages + 3 * kTiles;
   static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
-                                  kTiles * (size_t)kPBufBytes + kBars * 8 + 16;
+                                  kBars * 8 + 16;
 };
 
 template <typename T>
@@ -86,16 +85,6 @@ template <>
 struct Fmt<__nv_bfloat16> {
   static constexpr int v = 1;
 };
-
-// Packs 8 floats into 16-bit hi terms and their rounding residuals.
-template <typename T>
-__device__ __forceinline__ void pack8_split(const float* v, uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = Mma<T>::pack_split(v[2 * i], v[2 * i + 1], l[i]);
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -211,18 +200,15 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = base;                              // [tile][half][128 rows][128 B]
-  uint8_t* sKV = sQ + NT * C::kQBytes;             // [stage][K | V][half][64 rows][128 B]
-  uint8_t* sP = sKV + S * C::kStageBytes;          // [tile][hi | lo][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + NT * C::kPBufBytes);
+  uint8_t* sKV = sQ + NT * C::kQBytes;             // [stage][K | V][half][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + S;
   uint64_t* s_full = bars + 1 + 2 * S;  // [tile]
-  uint64_t* s_free = s_full + NT;
-  uint64_t* p_full = s_free + NT;
-  uint64_t* p_empty = p_full + NT;
-  uint64_t* o_full = p_empty + NT;
+  uint64_t* p_full = s_full + NT;
+  uint64_t* pv_done = p_full + NT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
@@ -260,10 +246,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(smem_addr(s_full + x), 1);
-      mbar_init(smem_addr(s_free + x), 128);
       mbar_init(smem_addr(p_full + x), 128);
-      mbar_init(smem_addr(p_empty + x), 1);
-      mbar_init(smem_addr(o_full + x), 1);
+      mbar_init(smem_addr(pv_done + x), 1);
     }
     fence_mbar_init();
   }
@@ -280,7 +264,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S of tile x at x * BN, O of tile x at NT * BN + x * D
+  // TMEM columns: S of tile x at x * BN (P_x is written over it), O of tile x at
+  // NT * BN + x * D.  P layout: 32-token chunk c of the row holds its 16-bit hi terms in
+  // columns 32c .. 32c+15 and its lo terms in 32c+16 .. 32c+31 (two tokens per column).
   bool ok = true;
 
   if (warp == 0) {
@@ -334,14 +320,14 @@ __global__ void __launch_bounds__(384, 1)
     if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // order: S_A(j), S_B(j), PV_A(j-1), PV_B(j-1), so that while one tile's softmax
-    // runs the tensor core works on the other tile
+    // Order: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ...  While one tile's softmax runs,
+    // the tensor core works through the other tile's P.V and next S.  S_x(j+1) reuses
+    // the TMEM columns PV_x(j) reads P from; tcgen05.mma operations issued by one thread
+    // execute in order, so no wait is needed between the two.
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM, BN, false, false);
       const uint32_t id_o = tc::idesc_f16(Fmt<T>::v, C::BM, D, false, true);
-      auto issue_s = [&](int x, int j) -> bool {
-        if (!mbar_wait(smem_addr(s_free + x), (j - 1) & 1)) return false;
-        tc::fence_after_sync();
+      auto issue_s = [&](int x, int j) {
         const uint32_t tS = tmem + x * BN;
         const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
         const uint32_t sk = smem_addr(sKV + (j % S) * C::kStageBytes);
@@ -353,40 +339,45 @@ __global__ void __launch_bounds__(384, 1)
           tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
         }
         tc::commit(smem_addr(s_full + x));
-        return true;
       };
-      auto issue_pv = [&](int x, int jj) -> bool {
-        if (!mbar_wait(smem_addr(p_full + x), jj & 1)) return false;
+      auto issue_pv = [&](int x, int j) -> bool {
+        if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
         tc::fence_after_sync();
+        const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint32_t sv = smem_addr(sKV + (jj % S) * C::kStageBytes + C::kKBytes);
-        const uint32_t sp = smem_addr(sP + x * C::kPBufBytes);
+        const uint32_t sv = smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
           const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
-          const uint64_t ahi = tc::smem_desc_sw128(sp + ks * 32, 16, 1024);
-          const uint64_t alo = tc::smem_desc_sw128(sp + C::kPBytes + ks * 32, 16, 1024);
-          tc::mma_f16_ss(tO, ahi, bdesc, id_o, jj > 0 || ks > 0);
-          tc::mma_f16_ss(tO, alo, bdesc, id_o, true);
+          tc::mma_f16_ts(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
+          tc::mma_f16_ts(tO, tP + col + 16, bdesc, id_o, true);
         }
-        tc::commit(smem_addr(p_empty + x));
-        if (jj == tg[x].n_kv - 1) tc::commit(smem_addr(o_full + x));
+        tc::commit(smem_addr(pv_done + x));
         return true;
       };
-      if (!mbar_wait(smem_addr(q_full), 0)) ok = false;
-      for (int j = 0; j <= n_kv && ok; ++j) {
-        if (j < n_kv) {
-          if (!mbar_wait(smem_addr(kv_full + j % S), (j / S) & 1)) { ok = false; break; }
+      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(kv_full), 0)) ok = false;
+      if (ok) {
+        tc::fence_after_sync();
 #pragma unroll
-          for (int x = 0; x < NT; ++x)
-            if (j < tg[x].n_kv && !issue_s(x, j)) ok = false;
-        }
-        if (j >= 1) {
+        for (int x = 0; x < NT; ++x)
+          if (tg[x].n_kv > 0) issue_s(x, 0);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        bool next_ready = false;
 #pragma unroll
-          for (int x = 0; x < NT; ++x)
-            if (j - 1 < tg[x].n_kv && ok && !issue_pv(x, j - 1)) ok = false;
-          tc::commit(smem_addr(kv_empty + (j - 1) % S));
+        for (int x = 0; x < NT; ++x) {
+          if (j < tg[x].n_kv && !issue_pv(x, j)) { ok = false; break; }
+          if (j + 1 < tg[x].n_kv) {
+            if (!next_ready) {
+              if (!mbar_wait(smem_addr(kv_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
+              tc::fence_after_sync();
+              next_ready = true;
+            }
+            issue_s(x, j + 1);
+          }
         }
+        tc::commit(smem_addr(kv_empty + j % S));
       }
       if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
@@ -400,37 +391,64 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tO = tmem + lane_bits + NT * BN + x * D;
     const TileGeom g = x == 0 ? tg[0] : tg[NT - 1];
     const int rpos = ctx0 + g.t0 + r / G;                    // position of this row's query
+    const int rpos_warp = ctx0 + g.t0 + (r & ~31) / G;       // smallest position in the warp
+    const float sc = p.scale_log2;
     float m = kNegInf, l = 0.f;
     for (int j = 0; j < g.n_kv; ++j) {
       if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      float xs[BN];
-      tc::tmem_ld32(tS, *reinterpret_cast<float(*)[32]>(xs));
-      tc::tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(xs + 32));
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      mbar_arrive(smem_addr(s_free + x));
-
       const int kp0 = j * BN;
+      const bool full = kp0 + BN - 1 <= rpos_warp;  // below the diagonal for the whole warp
+      // pass 1: row maximum of scale * S over the visible positions
       float mx = kNegInf;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        xs[c] = (kp0 + c <= rpos) ? xs[c] * p.scale_log2 : kNegInf;
-        mx = fmaxf(mx, xs[c]);
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        float a[32], bq[32];
+        tc::tmem_ld32(tS + c0, a);
+        tc::tmem_ld32(tS + c0 + 32, bq);
+        tc::tmem_wait_ld();
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(a[i], bq[i]) * sc);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            mx = fmaxf(mx, kp0 + c0 + i <= rpos ? a[i] * sc : kNegInf);
+            mx = fmaxf(mx, kp0 + c0 + 32 + i <= rpos ? bq[i] * sc : kNegInf);
+          }
+        }
       }
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
+      // pass 2: P = 2^(scale * S - m) as hi + lo 16-bit terms, over S's own columns
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        xs[c] = fast_exp2(xs[c] - m);
-        sum += xs[c];
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float a[32];
+        tc::tmem_ld32(tS + c0, a);
+        tc::tmem_wait_ld();
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            a[i] = kp0 + c0 + i <= rpos ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sum += a[2 * i] + a[2 * i + 1];
+          hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+        }
+        tc::tmem_st16(tS + c0, hi);
+        tc::tmem_st16(tS + c0 + 16, lo);
       }
       l = l * alpha + sum;
-      // the previous P.V must be complete before O is rescaled or P is overwritten
-      if (j >= 1 && !mbar_wait(smem_addr(p_empty + x), (j - 1) & 1)) { ok = false; break; }
       if (j >= 1 && __any_sync(~0u, need)) {
+        // O holds P_0..j-1 V: once the last of those products is done, rescale it
+        if (!mbar_wait(smem_addr(pv_done + x), (j - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -441,16 +459,6 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
           tc::tmem_st32(tO + c0, o);
         }
-        tc::tmem_wait_st();
-      }
-      const uint32_t sp = smem_addr(sP + x * C::kPBufBytes) + r * 128;
-#pragma unroll
-      for (int c8 = 0; c8 < BN / 8; ++c8) {
-        uint4 hi, lo;
-        pack8_split<T>(xs + 8 * c8, hi, lo);
-        const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
-        st_shared_v4(sp + off, hi);
-        st_shared_v4(sp + C::kPBytes + off, lo);
       }
       // V rows of the context's last K/V tile past the context (inside its last block)
       // may hold anything, NaN bits included, and would meet P = 0: zero them.  Both
@@ -465,13 +473,14 @@ __global__ void __launch_bounds__(384, 1)
           st_shared_v4(sv + (c >> 3) * C::kKvHalfBytes + vr * 128 + (c & 7) * 16,
                        make_uint4(0, 0, 0, 0));
         }
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(smem_addr(p_full + x));
     }
     // epilogue: O / l -> out rows
-    if (ok && g.n_kv > 0 && mbar_wait(smem_addr(o_full + x), 0)) {
+    if (ok && g.n_kv > 0 && mbar_wait(smem_addr(pv_done + x), (g.n_kv - 1) & 1)) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
       const int rows_valid = g.ntok * G;
