@@ -2,7 +2,8 @@
 """Benchmark of the paged decode step (KV GB/s, % of measured HBM peak, KV tokens/s).
 
 One step = the whole hot path over one batch: copy-on-write block copies (when the
-workload has them), slot mapping + cache write of every new token, then decode
+workload has them), slot mapping + cache write of every new token (one fused launch),
+then decode
 attention (plan, split-KV attention, merge) and chunked-prefill attention (when the
 workload has a prefill batch).  Default workload: the Llama-3.1-8B-shaped GQA decode
 layer (256 sequences, 32 query / 8 KV heads, head dim 128, bf16, block size 16,
@@ -207,10 +208,11 @@ def run_ours(args, rank, world, local_rank):
         if pairs is not None:
             pa.copy_blocks([kc], [vc], pairs)
             n += 1
-        for kind, m in meta.items():
-            pa.slot_mapping(m["slots"], m["bt"], m["cu"], m["ctx"], sh.block_size, step.num_blocks)
-            pa.reshape_and_cache(vals[f"k_new_{kind}"], vals[f"v_new_{kind}"], kc, vc, m["slots"])
-            n += 2
+        for kind, m in meta.items():  # slot mapping + cache write, fused
+            b = getattr(step, kind)
+            pa.cache_append(vals[f"k_new_{kind}"], vals[f"v_new_{kind}"], kc, vc, m["bt"], m["cu"],
+                            m["ctx"], b.max_q, m["slots"])
+            n += 1
         if d is not None:
             if ev is not None:
                 ev[0].record(stream)

@@ -107,6 +107,25 @@ int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, vo
                          void* stream);
 
 /*
+ * pa_cache_append -- slot mapping and cache write of a step's new tokens in one launch.
+ *
+ * Computes every new token's slot exactly as pa_slot_mapping does and writes its K and
+ * V there exactly as pa_reshape_and_cache does, without a slot array round trip.
+ *
+ *   k_new, v_new    [num_tokens, num_kv_heads, head_dim] of `dtype`, token t of sequence b
+ *                   at row cu_q_lens[b] + (t - cu_q_lens[b])
+ *   slots           int64 [num_tokens] receiving the slots (-1 for a rejected token), or
+ *                   NULL
+ *   max_q           bound on every sequence's new-token count cu_q_lens[b+1]-cu_q_lens[b]
+ * Other arguments as in pa_slot_mapping and pa_reshape_and_cache.  Bit-exact.
+ */
+int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    int64_t* slots, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                    int num_tokens, int max_q, int num_kv_heads, int head_dim, int block_size,
+                    int num_blocks, pa_dtype dtype, void* stream);
+
+/*
  * pa_copy_blocks -- copy-on-write of shared blocks.
  *
  * Sequences may share physical blocks; a shared block is copied only when one of them

@@ -21,7 +21,7 @@ from .build import LIB as LIB_PATH
 
 __all__ = [
     "PA_F32", "PA_F16", "PA_BF16", "PaError", "lib", "dtype_code",
-    "slot_mapping", "reshape_and_cache", "copy_blocks", "decode_workspace_bytes", "decode",
+    "slot_mapping", "reshape_and_cache", "cache_append", "copy_blocks", "decode_workspace_bytes", "decode",
     "prefill_workspace_bytes", "prefill_chunk", "get_status", "version",
     "STATUS_BAD_BLOCK", "STATUS_BAD_SLOT", "STATUS_BAD_CONTEXT", "STATUS_TIMEOUT",
 ]
@@ -52,6 +52,8 @@ _SIGNATURES = {
     "pa_slot_mapping": ([_p, _p, _i, _p, _p, _i, _i, _i, _i, _p], _i),
     "pa_reshape_and_cache": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _p], _i),
+    "pa_cache_append": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
+                         _p], _i),
     "pa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode": ([_p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz,
                    _p], _i),
@@ -132,6 +134,22 @@ def reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.T
     _check(lib().pa_reshape_and_cache(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                       _ptr(slots), k_new.shape[0], h_kv, d, bs, nb,
                                       dtype_code(k_cache.dtype), _stream(stream)))
+
+
+def cache_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, block_tables: torch.Tensor, cu_q_lens: torch.Tensor,
+                 context_lens: torch.Tensor, max_q: int, slots: Optional[torch.Tensor] = None,
+                 stream=None):
+    """Slot mapping and cache write of the step's new tokens in one launch."""
+    nb, h_kv, bs, d = k_cache.shape
+    _i32(block_tables, "block_tables")
+    if slots is not None and slots.dtype != torch.int64:
+        raise TypeError("slots must be int64")
+    _check(lib().pa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(slots), _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(cu_q_lens), _ptr(context_lens), context_lens.shape[0],
+                                 k_new.shape[0], max_q, h_kv, d, bs, nb,
+                                 dtype_code(k_cache.dtype), _stream(stream)))
 
 
 def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],

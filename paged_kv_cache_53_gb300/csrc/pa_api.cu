@@ -207,6 +207,35 @@ int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, vo
   return PA_OK;
 }
 
+int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    int64_t* slots, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                    int num_tokens, int max_q, int num_kv_heads, int head_dim, int block_size,
+                    int num_blocks, pa_dtype dtype, void* stream) {
+  g_error[0] = '\0';
+  if (num_tokens < 0 || num_seqs < 0 || max_q < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_cache_append: negative sizes");
+  int rc = check_cache_geometry("pa_cache_append", num_kv_heads, head_dim, block_size, num_blocks,
+                                dtype);
+  if (rc != PA_OK) return rc;
+  if (num_tokens == 0 || num_seqs == 0 || max_q == 0) return PA_OK;
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_cache_append: max_blocks_per_seq <= 0");
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !cu_q_lens || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "pa_cache_append: null pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "pa_cache_append: K/V pointers must be 16-byte aligned");
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_cache_append: no usable CUDA device");
+  cudaError_t e = launch_cache_append(k_new, v_new, k_cache, v_cache, slots, block_tables,
+                                      max_blocks_per_seq, cu_q_lens, context_lens, num_seqs,
+                                      num_tokens, max_q, num_kv_heads, head_dim, block_size,
+                                      num_blocks, dtype_bytes(dtype), st,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_cache_append: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                    const int32_t* pairs, int num_pairs, int num_kv_heads, int head_dim,
                    int block_size, int num_blocks, pa_dtype dtype, void* stream) {

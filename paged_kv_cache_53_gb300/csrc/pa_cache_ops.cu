@@ -75,6 +75,58 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k_new,
   v_cache[dst] = __ldg(v_new + src);
 }
 
+// Slot mapping fused with the cache write: CTA (x, b) takes up to kAppendTokens new
+// tokens of sequence b, computes their slots, then moves their K and V rows in 16-byte
+// chunks with all of its threads.
+constexpr int kAppendTokens = 8;
+
+__global__ void __launch_bounds__(256) cache_append_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, int64_t* __restrict__ slots_out,
+    const int32_t* __restrict__ block_tables, int max_blocks, const int32_t* __restrict__ cu_q_lens,
+    const int32_t* __restrict__ context_lens, int num_tokens, int num_kv_heads,
+    int chunks_per_row, int block_size, int num_blocks, int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ long long s_slot[kAppendTokens];
+  const int b = blockIdx.y;
+  const int first = __ldg(cu_q_lens + b);
+  const int n_new = __ldg(cu_q_lens + b + 1) - first;
+  const int i0 = blockIdx.x * kAppendTokens;
+  if (i0 >= n_new) return;
+  const int nt = min(kAppendTokens, n_new - i0);
+  if (threadIdx.x < nt) {
+    const int i = i0 + threadIdx.x;
+    const long long t = (long long)first + i;
+    long long slot = -1;
+    const long long pos = (long long)__ldg(context_lens + b) - n_new + i;
+    if (t < 0 || t >= num_tokens || pos < 0 || pos >= (long long)max_blocks * block_size) {
+      flag_status(status, PA_STATUS_BAD_CONTEXT);
+    } else {
+      const int blk = __ldg(block_tables + (size_t)b * max_blocks + pos / block_size);
+      if (blk < 0 || blk >= num_blocks)
+        flag_status(status, PA_STATUS_BAD_BLOCK);
+      else
+        slot = (long long)blk * block_size + pos % block_size;
+    }
+    s_slot[threadIdx.x] = slot;
+    if (slots_out != nullptr && t >= 0 && t < num_tokens) slots_out[t] = slot;
+  }
+  __syncthreads();
+  const int per_tok = num_kv_heads * chunks_per_row;
+  for (int c = threadIdx.x; c < nt * per_tok; c += blockDim.x) {
+    const int ti = c / per_tok, rem = c - ti * per_tok;
+    const long long slot = s_slot[ti];
+    if (slot < 0) continue;
+    const int h = rem / chunks_per_row, cc = rem - h * chunks_per_row;
+    const long long blk = slot / block_size, off = slot - blk * block_size;
+    const long long dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + cc;
+    const long long src = ((long long)(first + i0 + ti) * num_kv_heads + h) * chunks_per_row + cc;
+    k_cache[dst] = __ldg(k_new + src);
+    v_cache[dst] = __ldg(v_new + src);
+  }
+}
+
 struct LayerPtrs {
   uint4* k[kMaxCopyLayers];
   uint4* v[kMaxCopyLayers];
@@ -126,6 +178,23 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void*
                     static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots,
                     num_tokens, num_kv_heads, chunks_per_row, block_size,
                     (long long)num_blocks * block_size, status);
+}
+
+cudaError_t launch_cache_append(const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, int64_t* slots, const int32_t* block_tables,
+                                int max_blocks, const int32_t* cu_q_lens,
+                                const int32_t* context_lens, int num_seqs, int num_tokens,
+                                int max_q, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, size_t elem_bytes, int32_t* status,
+                                cudaStream_t stream) {
+  const int chunks_per_row = (int)(head_dim * elem_bytes / 16);
+  const int gx = (max_q + kAppendTokens - 1) / kAppendTokens;
+  if (num_seqs > 65535) return cudaErrorInvalidValue;
+  return launch_pdl(cache_append_kernel, dim3(gx, num_seqs), dim3(256), 0, stream,
+                    static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots,
+                    block_tables, max_blocks, cu_q_lens, context_lens, num_tokens, num_kv_heads,
+                    chunks_per_row, block_size, num_blocks, status);
 }
 
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,

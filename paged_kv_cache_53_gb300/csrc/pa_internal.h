@@ -48,6 +48,14 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, void*
                                      int num_blocks, size_t elem_bytes, int32_t* status,
                                      cudaStream_t stream);
 
+cudaError_t launch_cache_append(const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, int64_t* slots, const int32_t* block_tables,
+                                int max_blocks, const int32_t* cu_q_lens,
+                                const int32_t* context_lens, int num_seqs, int num_tokens,
+                                int max_q, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, size_t elem_bytes, int32_t* status,
+                                cudaStream_t stream);
+
 constexpr int kMaxCopyLayers = 256;
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                                const int32_t* pairs, int num_pairs, size_t block_bytes,

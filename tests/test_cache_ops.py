@@ -103,3 +103,42 @@ def test_copy_blocks_skips_pairs_outside_the_pool(pa):
     assert pa.get_status() & pa.STATUS_BAD_BLOCK
     ref[3] = ref[2]
     assert torch.equal(kc, ref)
+
+
+@pytest.mark.parametrize("query_lens,ctx,bs,dtype", [
+    ([1, 1, 1, 1], [1, 16, 17, 100], 16, "bf16"),
+    ([5, 16, 1, 33], [5, 40, 33, 200], 16, "f16"),
+    ([512, 1, 9], [512, 7, 16896], 32, "bf16"),
+    ([0, 3, 0], [10, 3, 1], 16, "f32"),
+])
+def test_cache_append_bit_exact(pa, query_lens, ctx, bs, dtype):
+    """Slot mapping fused with the cache write gives the same slots and pool as the two
+    separate operations of the oracle."""
+    step = W.prefill_step("a", W.Shape(8, 4, 128, bs, dtype), ctx, query_lens, seed=5)
+    b = step.prefill
+    vals = W.make_values(step, "cuda")
+    kc0, vc0 = W.to_numpy(vals["k_cache"]), W.to_numpy(vals["v_cache"])
+    slots = torch.full((b.num_new_tokens,), -7, dtype=torch.int64, device="cuda")
+    pa.cache_append(vals["k_new_prefill"], vals["v_new_prefill"], vals["k_cache"],
+                    vals["v_cache"], _dev(b.block_tables), _dev(b.cu_q_lens),
+                    _dev(b.context_lens), b.max_q, slots)
+    ref = oracle.slot_mapping(b.block_tables, b.cu_q_lens, b.context_lens, bs)
+    oracle.reshape_and_cache(W.to_numpy(vals["k_new_prefill"]), W.to_numpy(vals["v_new_prefill"]),
+                             kc0, vc0, ref)
+    assert np.array_equal(slots.cpu().numpy(), ref)
+    assert np.array_equal(W.to_numpy(vals["k_cache"]), kc0)
+    assert np.array_equal(W.to_numpy(vals["v_cache"]), vc0)
+    assert pa.get_status() == 0
+
+
+def test_cache_append_without_slot_output(pa):
+    step = W.decode_step("a2", W.Shape(32, 8, 128, 16, "bf16"), [1, 17, 300], seed=6)
+    b = step.decode
+    vals = W.make_values(step, "cuda")
+    kc0 = W.to_numpy(vals["k_cache"])
+    pa.cache_append(vals["k_new_decode"], vals["v_new_decode"], vals["k_cache"], vals["v_cache"],
+                    _dev(b.block_tables), _dev(b.cu_q_lens), _dev(b.context_lens), 1)
+    ref = oracle.slot_mapping(b.block_tables, b.cu_q_lens, b.context_lens, 16)
+    oracle.reshape_and_cache(W.to_numpy(vals["k_new_decode"]), W.to_numpy(vals["v_new_decode"]),
+                             kc0, kc0.copy(), ref)
+    assert np.array_equal(W.to_numpy(vals["k_cache"]), kc0)
