@@ -15,8 +15,8 @@
 //                m16n8k16, the query group padded to 16 rows) with an online softmax.
 //                A unit covering a whole context writes the normalised output; the
 //                others write an fp32 partial (running max, sum, unnormalised output).
-//   3. merge  -- one warp per (sequence, KV head) with more than one partition merges
-//                its partials by log-sum-exp rescaling.  (Merging inside the attention
+//   3. merge  -- one warp per (sequence, query head) with more than one partition
+//                merges its partials by log-sum-exp rescaling.  (Merging inside the attention
 //                kernel, by whichever warp finished last, stalled that warp's pipeline
 //                on a device-wide fence and an atomic round trip per partition, which
 //                cost more than this launch.)
@@ -214,112 +214,79 @@ __device__ __forceinline__ void combine_ml(float& m, float& l, float m2, float l
 
 constexpr int kMaxGroup = 16;
 
-// Merges the partials of one (sequence, KV head) once all of them are written:
+// Merges the partials of one (sequence, query head):
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p with M = max_p m_p.  Run by one
 // warp; each lane owns D/32 consecutive columns.  Two dependent rounds of loads: the
-// (max, sum) of every partition and group row, then every partial output row; the rows
-// of all partitions are in flight together.  Partials written by other CTAs are read
-// through L2 (ld.global.cg).
+// (max, sum) of every partition, then every partial output row, all in flight together.
+// The partials were written by the previous kernel and are read through L2.
 template <int D, typename TO>
-__device__ __forceinline__ void merge_partials(const DecodeParams& p, const UnitDesc& d, TO* out,
-                                               int lane) {
+__device__ __forceinline__ void merge_row(const DecodeParams& p, int b, int hq, int ps, int np,
+                                          TO* out, int lane) {
   constexpr int C = D / 32;
-  const int G = p.group;
-  const int np = d.nparts;
   const size_t hs = (size_t)p.num_q_heads;
-  const int hq0 = d.h * G;
-  const float2* ml = p.ws.part_ml + (size_t)d.part_start * hs + hq0;  // [partition][g]
-  const float* acc_base = p.ws.part_acc + ((size_t)d.part_start * hs + hq0) * D + lane * C;
-  float M[kMaxGroup], L[kMaxGroup], m_own[kMaxGroup];
-#pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g) {
-    M[g] = kNegInf;
-    L[g] = 0.f;
-    m_own[g] = kNegInf;
-  }
-  // round 1: lane i folds partitions i, i + 32, ... of every row into (max, sum)
+  const float2* ml = p.ws.part_ml + (size_t)ps * hs + hq;  // stride hs per partition
+  float M = kNegInf, L = 0.f, m_own = kNegInf;
   for (int i0 = 0; i0 < np; i0 += 32) {
     const int i = i0 + lane;
     if (i < np) {
-#pragma unroll
-      for (int g = 0; g < kMaxGroup; ++g) {
-        if (g >= G) break;
-        const float2 v = __ldcg(ml + i * hs + g);
-        if (i0 == 0) m_own[g] = v.x;
-        combine_ml(M[g], L[g], v.x, v.y);
-      }
+      const float2 v = __ldcg(ml + i * hs);
+      if (i0 == 0) m_own = v.x;
+      combine_ml(M, L, v.x, v.y);
     }
   }
 #pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g) {
-    if (g >= G) break;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(~0u, M[g], o);
-      const float l2 = __shfl_xor_sync(~0u, L[g], o);
-      combine_ml(M[g], L[g], m2, l2);
-    }
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(~0u, M, o);
+    const float l2 = __shfl_xor_sync(~0u, L, o);
+    combine_ml(M, L, m2, l2);
   }
-  // round 2: weighted sum of the partial outputs
-#pragma unroll 1
-  for (int g = 0; g < G; ++g) {
-    float mg = 0.f, own = kNegInf;
+  float acc[C];
 #pragma unroll
-    for (int k = 0; k < kMaxGroup; ++k)
-      if (k == g) { mg = M[k]; own = m_own[k]; }
-    float acc[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.f;
-    for (int i0 = 0; i0 < np; i0 += 32) {
-      const int i = i0 + lane;
-      float w = 0.f;
-      if (i < np) w = fast_exp2((i0 == 0 ? own : __ldcg(ml + i * hs + g).x) - mg);
-      const int n = min(32, np - i0);
+  for (int c = 0; c < C; ++c) acc[c] = 0.f;
+  const float* src = p.ws.part_acc + ((size_t)ps * hs + hq) * D + lane * C;
+  for (int i0 = 0; i0 < np; i0 += 32) {
+    const int i = i0 + lane;
+    float w = 0.f;
+    if (i < np) w = fast_exp2((i0 == 0 ? m_own : __ldcg(ml + i * hs).x) - M);
+    const int n = min(32, np - i0);
 #pragma unroll 8
-      for (int j = 0; j < n; ++j) {
-        const float wj = __shfl_sync(~0u, w, j);
-        const float* row = acc_base + ((size_t)(i0 + j) * hs + g) * D;
-        if constexpr (C == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(row));
-          acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(row));
-          acc[0] += wj * v.x; acc[1] += wj * v.y;
-        }
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(~0u, w, j);
+      const float* row = src + (size_t)(i0 + j) * hs * D;
+      if constexpr (C == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(row));
+        acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(row));
+        acc[0] += wj * v.x; acc[1] += wj * v.y;
       }
     }
-    float lg = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxGroup; ++k)
-      if (k == g) lg = L[k];
-    const float inv = 1.f / lg;
-    TO* o = out + ((size_t)d.b * p.num_q_heads + hq0 + g) * D + lane * C;
-#pragma unroll
-    for (int c = 0; c < C; c += 2) store2(o + c, acc[c] * inv, acc[c + 1] * inv);
   }
+  const float inv = 1.f / L;
+  TO* o = out + ((size_t)b * p.num_q_heads + hq) * D + lane * C;
+#pragma unroll
+  for (int c = 0; c < C; c += 2) store2(o + c, acc[c] * inv, acc[c + 1] * inv);
 }
 
-// 3. merge: one warp per (sequence, KV head) with more than one partition.
+// 3. merge: one warp per (sequence, query head) of a sequence with several partitions.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, int head_dim) {
   griddep_wait();  // every partial of the attention kernel is written
   griddep_launch_dependents();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= p.num_seqs * p.num_kv_heads) return;
-  UnitDesc d;
-  d.b = w / p.num_kv_heads;
-  d.h = w - d.b * p.num_kv_heads;
-  d.part_start = p.ws.part_start[d.b];
-  d.nparts = p.ws.part_start[d.b + 1] - d.part_start;
-  if (d.nparts <= 1) return;  // written by the attention kernel (or zeroed by the plan)
+  if (w >= p.num_seqs * p.num_q_heads) return;
+  const int b = w / p.num_q_heads, hq = w - b * p.num_q_heads;
+  const int ps = p.ws.part_start[b];
+  const int np = p.ws.part_start[b + 1] - ps;
+  if (np <= 1) return;  // written by the attention kernel (or zeroed by the plan)
   if (head_dim == 128) {
-    if (p.out_f32 || p.out_bytes == 4) merge_partials<128, float>(p, d, static_cast<float*>(p.out), lane);
-    else if (p.out_bf16) merge_partials<128, __nv_bfloat16>(p, d, static_cast<__nv_bfloat16*>(p.out), lane);
-    else merge_partials<128, __half>(p, d, static_cast<__half*>(p.out), lane);
+    if (p.out_bytes == 4) merge_row<128, float>(p, b, hq, ps, np, static_cast<float*>(p.out), lane);
+    else if (p.out_bf16) merge_row<128, __nv_bfloat16>(p, b, hq, ps, np, static_cast<__nv_bfloat16*>(p.out), lane);
+    else merge_row<128, __half>(p, b, hq, ps, np, static_cast<__half*>(p.out), lane);
   } else {
-    if (p.out_f32 || p.out_bytes == 4) merge_partials<64, float>(p, d, static_cast<float*>(p.out), lane);
-    else if (p.out_bf16) merge_partials<64, __nv_bfloat16>(p, d, static_cast<__nv_bfloat16*>(p.out), lane);
-    else merge_partials<64, __half>(p, d, static_cast<__half*>(p.out), lane);
+    if (p.out_bytes == 4) merge_row<64, float>(p, b, hq, ps, np, static_cast<float*>(p.out), lane);
+    else if (p.out_bf16) merge_row<64, __nv_bfloat16>(p, b, hq, ps, np, static_cast<__nv_bfloat16*>(p.out), lane);
+    else merge_row<64, __half>(p, b, hq, ps, np, static_cast<__half*>(p.out), lane);
   }
 }
 
@@ -909,7 +876,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     rc = launch_mma_dispatch<__half>(a, p, stream);
   }
   if (rc != PA_OK) return rc;
-  const int warps = a.num_seqs * a.num_kv_heads;
+  const int warps = a.num_seqs * a.num_q_heads;
   e = launch_pdl(decode_merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, stream, p, a.head_dim);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (merge): %s", cudaGetErrorString(e));
   return PA_OK;
