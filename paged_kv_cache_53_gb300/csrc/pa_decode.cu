@@ -144,13 +144,30 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     ws.part_start[b] = run;
     run += (clamp_ctx(context_lens[b], ctx_cap) + psz - 1) / psz;
   }
-  if (tid == 0) {
-    ws.part_start[num_seqs] = s_total;
-    int acc = 0;  // bucket offsets, largest partitions first
-    for (int k = bpp; k >= 1; --k) {
-      const int h = s_hist[k];
-      s_hist[k] = acc;
-      acc += h;
+  if (tid == 0) ws.part_start[num_seqs] = s_total;
+  if (wid == 0) {
+    // bucket offsets, largest partitions first: an exclusive scan of s_hist[bpp .. 1]
+    // by one warp, each lane owning kMaxPartBlocks / 32 consecutive buckets
+    constexpr int per = kMaxPartBlocks / 32;
+    int v[per], run = 0;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      const int bucket = bpp - (lane * per + k);
+      v[k] = bucket >= 1 ? s_hist[bucket] : 0;
+      run += v[k];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(~0u, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int off = incl - run;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      const int bucket = bpp - (lane * per + k);
+      if (bucket >= 1) s_hist[bucket] = off;
+      off += v[k];
     }
   }
   __syncthreads();
