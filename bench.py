@@ -107,6 +107,28 @@ def recorded_traffic(workload: str):
     return None
 
 
+# ------------------------------------------------------------------ ranks
+def replica_step(workload: str, rank: int, world: int) -> W.Step:
+    """The step rank `rank` serves: the named workload, reseeded per rank so that each
+    replica holds its own batch (sequences are independent; no data crosses ranks)."""
+    step = W.NAMED[workload]()
+    if world > 1:
+        step = W.replace(step, seed=step.seed + 1000 * rank)
+    return step
+
+
+def slowest_over_ranks(values, world: int, device=None):
+    """Element-wise maximum over all ranks of per-rank times: the slowest rank sets the
+    job's time.  The only collective of the bench, outside the timed region."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu().tolist()]
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -166,9 +188,7 @@ def run_ours(args, rank, world, local_rank):
     pabuild.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    step = W.NAMED[args.workload]()
-    if world > 1:  # each rank serves its own batch: independent units, no exchange
-        step = W.replace(step, seed=step.seed + 1000 * rank)
+    step = replica_step(args.workload, rank, world)
     sh = step.shape
     vals = W.make_values(step, dev)
     kc, vc = vals["k_cache"], vals["v_cache"]
@@ -303,13 +323,8 @@ def run_ours(args, rank, world, local_rank):
     q_in.update(saved[1])
 
     step_ms = total_ms / k
-    times = np.array([step_ms, dec_ms, pre_ms, e2e_ms], dtype=np.float64)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor(times, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        times = t.cpu().numpy()
-    step_ms, dec_ms, pre_ms, e2e_ms = [float(x) for x in times]
+    step_ms, dec_ms, pre_ms, e2e_ms = slowest_over_ranks([step_ms, dec_ms, pre_ms, e2e_ms], world,
+                                                         device=dev)
 
     config = {
         "workload": step.name, "num_q_heads": sh.num_q_heads, "num_kv_heads": sh.num_kv_heads,
