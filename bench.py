@@ -51,14 +51,30 @@ def kv_bytes(step: W.Step) -> int:
         sh.head_dim * sh.elem_bytes
 
 
-def decode_algorithmic_bytes(step: W.Step, out_bytes: int) -> int:
+def shared_prefix_saving(step: W.Step):
+    """(tokens, blocks) that a decode attending the shared prefix once does not read
+    again: the prefix of every sharer after the first."""
+    if step.shared_prefix is None:
+        return 0, 0
+    _, plen, sharers = step.shared_prefix
+    extra = max(0, len(sharers) - 1)
+    return extra * plen, extra * (plen // step.shape.block_size)
+
+
+def decode_algorithmic_bytes(step: W.Step, out_bytes: int, shared: bool = False) -> int:
     """Algorithmic HBM bytes of one decode call: KV rows, q, the output, the block-table
-    entries walked and the context lengths."""
+    entries walked and the context lengths.  With `shared`, the shared prefix's KV rows
+    and block entries count once."""
     sh, b = step.shape, step.decode
     blocks = int(((b.context_lens.astype(np.int64) + sh.block_size - 1) // sh.block_size).sum())
     q = b.num_seqs * sh.num_q_heads * sh.head_dim * sh.elem_bytes
     o = b.num_seqs * sh.num_q_heads * sh.head_dim * out_bytes
-    return kv_bytes(step) + q + o + 4 * blocks + 4 * b.num_seqs
+    kv = kv_bytes(step)
+    if shared:
+        tok, blk = shared_prefix_saving(step)
+        kv -= tok * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+        blocks -= blk
+    return kv + q + o + 4 * blocks + 4 * b.num_seqs
 
 
 def prefill_useful_flops(step: W.Step) -> int:
@@ -208,12 +224,20 @@ def run_ours(args, rank, world, local_rank):
         }
     pairs = torch.from_numpy(step.cow_pairs).to(dev) if step.cow_pairs is not None else None
     d, p = step.decode, step.prefill
+    share = d is not None and step.shared_prefix is not None and args.share_prefix == "on"
     if d is not None:
         out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
-        ws_dec = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads,
-                                                       sh.num_kv_heads, sh.head_dim, d.max_ctx,
-                                                       sh.block_size),
-                             dtype=torch.uint8, device=dev)
+        if share:
+            pblocks, plen, sharers = step.shared_prefix
+            meta["decode"]["pblocks"] = torch.from_numpy(pblocks).to(dev)
+            meta["decode"]["sharers"] = torch.from_numpy(sharers).to(dev)
+            nbytes = pa.decode_shared_prefix_workspace_bytes(
+                d.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, d.max_ctx,
+                sh.block_size, len(sharers), plen)
+        else:
+            nbytes = pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads, sh.num_kv_heads,
+                                               sh.head_dim, d.max_ctx, sh.block_size)
+        ws_dec = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     if p is not None:
         out_pre = torch.empty((p.num_new_tokens, sh.num_q_heads, sh.head_dim), dtype=tdt,
                               device=dev)
@@ -239,11 +263,18 @@ def run_ours(args, rank, world, local_rank):
         if d is not None:
             if ev is not None:
                 ev[0].record(stream)
-            pa.decode(out_dec, q_in["decode"], kc, vc, meta["decode"]["bt"],
-                      meta["decode"]["ctx"], d.max_ctx, step.scale, ws_dec)
+            md = meta["decode"]
+            if share:
+                pa.decode_shared_prefix(out_dec, q_in["decode"], kc, vc, md["bt"], md["ctx"],
+                                        d.max_ctx, md["pblocks"], plen, md["sharers"],
+                                        step.scale, ws_dec)
+                n += 4  # plan, shared prefix, attend, merge
+            else:
+                pa.decode(out_dec, q_in["decode"], kc, vc, md["bt"], md["ctx"], d.max_ctx,
+                          step.scale, ws_dec)
+                n += 3  # plan, attend, merge
             if ev is not None:
                 ev[1].record(stream)
-            n += 3  # plan, attend, merge
         if p is not None:
             if ev is not None:
                 ev[2].record(stream)
@@ -289,7 +320,8 @@ def run_ours(args, rank, world, local_rank):
     # end to end: the step's inputs from pinned host memory, the outputs back to the host
     h_in = {key: vals[key].cpu().pin_memory() for key in vals
             if key.startswith(("q_", "k_new", "v_new"))}
-    h_meta = {kind: {n: m[n].cpu().pin_memory() for n in ("bt", "ctx", "cu")}
+    h_meta = {kind: {n: m[n].cpu().pin_memory()
+                     for n in ("bt", "ctx", "cu", "pblocks", "sharers") if n in m}
               for kind, m in meta.items()}
     outs = ([out_dec] if d is not None else []) + ([out_pre] if p is not None else [])
     h_outs = [torch.empty(o.shape, dtype=tdt).pin_memory() for o in outs]
@@ -332,6 +364,9 @@ def run_ours(args, rank, world, local_rank):
         "cow_copies": int(step.cow_pairs.shape[0]) if step.cow_pairs is not None else 0,
         "parallelism": f"replicas x{world}",
     }
+    if share:
+        config["shared_prefix"] = {"sharers": int(len(sharers)), "prefix_len": int(plen),
+                                   "attended": "once per KV head for all sharers"}
     res = {"metric": METRIC, "n_gpus": world, "steps": k, "warmup": args.warmup,
            "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": sh.dtype, "data": "synthetic", "config": config}
@@ -348,7 +383,7 @@ def run_ours(args, rank, world, local_rank):
         kvb = kv_bytes(step)
         kv_tokens = int(d.context_lens.astype(np.int64).sum())
         peak, peak_kind = measured_peaks()
-        alg = decode_algorithmic_bytes(step, out_dec.element_size())
+        alg = decode_algorithmic_bytes(step, out_dec.element_size(), shared=share)
         achieved = alg / (dec_ms * 1e-3) / 1e9
         config.update({"num_seqs": d.num_seqs, "kv_tokens_per_step": kv_tokens,
                        "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
@@ -361,10 +396,13 @@ def run_ours(args, rank, world, local_rank):
             "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5), "steps": ke},
-            "roofline": {"bound": "hbm", "kernel": "pa_decode (plan + attend + merge)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("pa_decode_shared_prefix (plan + shared prefix + attend + "
+                                    "merge)" if share else "pa_decode (plan + attend + merge)"),
                          "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": recorded_traffic(args.workload), "algorithmic_bytes": alg,
+                         "traffic": None if share else recorded_traffic(args.workload),
+                         "algorithmic_bytes": alg,
                          "ms_per_launch": round(dec_ms, 5)},
         })
         if p is not None:
@@ -542,6 +580,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.NAMED), default="llama8b_gqa_decode")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--share-prefix", choices=["on", "off"], default="on",
+                    help="workloads with a shared prefix: attend it once for all sharers "
+                         "(pa_decode_shared_prefix) or per sequence (pa_decode)")
     ap.add_argument("--cpu-budget-s", type=float, default=2.0,
                     help="seconds per core of oracle work for the cpu_baseline sample")
     ap.add_argument("--ref-total-s", type=float, default=120.0,

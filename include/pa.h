@@ -181,6 +181,41 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_shared_prefix -- pa_decode for a batch in which some sequences share one
+ * physical prefix.
+ *
+ * Sequences may point their tables at the same physical blocks when they share a prompt
+ * prefix ("Continuous batching, paged attention, prefix caching", section "Prefix
+ * caching": the server keeps one physical copy and points both block tables at it).
+ * The result is exactly pa_decode's; the work differs: the prefix's attention is
+ * computed once per KV head for all the sequences reading it, as one dense contraction
+ * of all their query groups with the prefix's K/V on the tensor cores, and merged with
+ * each sequence's own remaining context by log-sum-exp rescaling.  The prefix's K/V are
+ * read from HBM once instead of once per sequence.
+ *
+ *   prefix_blocks  int32 [prefix_len / block_size], the prefix's physical blocks, device
+ *   prefix_len     tokens of the prefix, a multiple of block_size
+ *   sharers        int32 [num_sharers], distinct indices of the sequences (rows of
+ *                  block_tables) whose first prefix_len tokens are that prefix; each must
+ *                  have context_lens >= prefix_len and its table must start with
+ *                  prefix_blocks (not checked)
+ *   workspace      at least pa_decode_shared_prefix_workspace_bytes(...) bytes
+ * Other arguments as in pa_decode; dtype PA_F16 or PA_BF16.  num_sharers = 0 (or
+ * prefix_len = 0) is a plain decode.
+ */
+size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int max_ctx, int block_size,
+                                               int num_sharers, int prefix_len);
+int pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens, int max_ctx,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, const int32_t* prefix_blocks,
+                            int prefix_len, const int32_t* sharers, int num_sharers, float scale,
+                            pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * pa_decode_static_scratch -- pa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call; it exists for integration.  A caller that

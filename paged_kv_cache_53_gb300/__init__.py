@@ -21,7 +21,8 @@ from .build import LIB as LIB_PATH
 
 __all__ = [
     "PA_F32", "PA_F16", "PA_BF16", "PaError", "lib", "dtype_code",
-    "slot_mapping", "reshape_and_cache", "cache_append", "copy_blocks", "decode_workspace_bytes", "decode",
+    "slot_mapping", "reshape_and_cache", "cache_append", "copy_blocks", "decode_workspace_bytes",
+    "decode", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
     "prefill_workspace_bytes", "prefill_chunk", "get_status", "version",
     "STATUS_BAD_BLOCK", "STATUS_BAD_SLOT", "STATUS_BAD_CONTEXT", "STATUS_TIMEOUT",
 ]
@@ -55,6 +56,9 @@ _SIGNATURES = {
     "pa_cache_append": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                          _p], _i),
     "pa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
+    "pa_decode_shared_prefix_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
+    "pa_decode_shared_prefix": ([_p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i,
+                                 _p, _i, _p, _i, _f, _i, _p, _sz, _p], _i),
     "pa_decode": ([_p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz,
                    _p], _i),
     "pa_prefill_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
@@ -183,6 +187,33 @@ def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
                            _ptr(context_lens), max_ctx, b, h_q, h_kv, d, bs, nb, float(scale),
                            dtype_code(k_cache.dtype), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                         head_dim: int, max_ctx: int, block_size: int,
+                                         num_sharers: int, prefix_len: int) -> int:
+    return int(lib().pa_decode_shared_prefix_workspace_bytes(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size, num_sharers,
+        prefix_len))
+
+
+def decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, max_ctx: int, prefix_blocks: torch.Tensor,
+                         prefix_len: int, sharers: torch.Tensor, scale: float,
+                         workspace: torch.Tensor, stream=None):
+    """pa_decode with the prefix shared by the rows in `sharers` attended once per KV head
+    (see pa_decode_shared_prefix)."""
+    nb, h_kv, bs, d = k_cache.shape
+    b, h_q, _ = q.shape
+    _i32(prefix_blocks, "prefix_blocks")
+    _i32(sharers, "sharers")
+    _check(lib().pa_decode_shared_prefix(
+        _ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), max_ctx, b, h_q, h_kv, d,
+        bs, nb, _ptr(prefix_blocks), prefix_len, _ptr(sharers), sharers.shape[0], float(scale),
+        dtype_code(k_cache.dtype), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def prefill_workspace_bytes(num_seqs: int, num_tokens: int, max_q: int, num_q_heads: int,

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpagedattn.so")
 SOURCES = ["pa_api.cu", "pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu",
-           "pa_decode_static.cu"]
+           "pa_decode_static.cu", "pa_shared_prefix.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -329,6 +329,97 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
   a.ws = carve_decode_workspace(workspace, num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
                                 block_size);
   a.status = st;
+  a.prefix = PrefixPlan{};
+  return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+// Partial slots the prefix's splits add to the decode workspace (none without sharers,
+// which also leaves the workspace without per-sequence prefix flags).
+static long long prefix_slots(const PrefixPlan& pp) {
+  return pp.num_sharers > 0 ? (long long)pp.num_sharers * pp.splits : 0;
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int max_ctx, int block_size,
+                                               int num_sharers, int prefix_len) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_ctx < 0 ||
+      block_size <= 0 || num_sharers < 0 || prefix_len < 0 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  const PrefixPlan pp =
+      plan_prefix(num_sharers, prefix_len, num_q_heads / num_kv_heads, num_kv_heads);
+  return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size, prefix_slots(pp));
+}
+
+int pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens, int max_ctx,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, const int32_t* prefix_blocks,
+                            int prefix_len, const int32_t* sharers, int num_sharers, float scale,
+                            pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  g_error[0] = '\0';
+  int rc = check_cache_geometry("pa_decode_shared_prefix", num_kv_heads, head_dim, block_size,
+                                num_blocks, dtype);
+  if (rc != PA_OK) return rc;
+  if (dtype == PA_F32)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: fp16/bf16 only (tensor cores)");
+  if (num_seqs < 0 || max_ctx < 0 || num_q_heads <= 0 || num_sharers < 0 || prefix_len < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_shared_prefix: negative sizes");
+  if (num_seqs == 0) return PA_OK;
+  if (!valid_dtype(out_dtype) || (out_dtype != dtype && out_dtype != PA_F32))
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_decode_shared_prefix: out_dtype must equal dtype or be PA_F32");
+  if (num_q_heads % num_kv_heads != 0 || !supported_group(num_q_heads / num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: group size not built");
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_shared_prefix: max_blocks_per_seq <= 0");
+  if (prefix_len % block_size != 0 || prefix_len > max_ctx)
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_decode_shared_prefix: prefix_len %d must be a multiple of the block size "
+                "and <= max_ctx",
+                prefix_len);
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode_shared_prefix: scale is NaN");
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace ||
+      (num_sharers > 0 && prefix_len > 0 && (!sharers || !prefix_blocks)))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_shared_prefix: null pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace))
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_decode_shared_prefix: out/q/caches/workspace must be 16-byte aligned");
+  const size_t need = pa_decode_shared_prefix_workspace_bytes(
+      num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size, num_sharers,
+      prefix_len);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "pa_decode_shared_prefix: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: no usable CUDA device");
+  DecodeArgs a;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_ctx = max_ctx;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.prefix = plan_prefix(num_sharers, prefix_len, num_q_heads / num_kv_heads, num_kv_heads);
+  a.prefix.sharers = sharers;
+  a.prefix.prefix_blocks = prefix_blocks;
+  a.ws = carve_decode_workspace(workspace, num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size, prefix_slots(a.prefix));
+  a.status = st;
   return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 

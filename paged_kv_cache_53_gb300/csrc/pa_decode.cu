@@ -72,23 +72,45 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
                                                            int num_seqs, int ctx_cap,
                                                            int num_kv_heads, int block_size,
                                                            DecodeWorkspace ws, int32_t* status,
-                                                           int4* out, int out_row_vec16) {
+                                                           int4* out, int out_row_vec16,
+                                                           PrefixPlan pre) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ long long s_sum[32];
   __shared__ int s_off[32];
   __shared__ int s_hist[kMaxPartBlocks + 2];
-  __shared__ int s_psz, s_total;
+  __shared__ int s_psz, s_total, s_units;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
   const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+
+  // sequences reading a shared prefix start their own partitions after it and keep
+  // pre.splits partial slots, ahead of those, for the prefix's partials
+  if (pre.num_sharers > 0) {
+    for (int b = tid; b < num_seqs; b += blockDim.x) ws.seq_flags[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < pre.num_sharers; i += blockDim.x) {
+      const int sb = pre.sharers[i];
+      if (sb >= 0 && sb < num_seqs) ws.seq_flags[sb] = 1;
+      else flag_status(status, PA_STATUS_BAD_CONTEXT);
+    }
+    __syncthreads();
+  }
+  auto start_of = [&](int b) {
+    return (pre.num_sharers > 0 && ws.seq_flags[b]) ? pre.prefix_len : 0;
+  };
+  auto reserved_of = [&](int b) {
+    return (pre.num_sharers > 0 && ws.seq_flags[b]) ? pre.splits : 0;
+  };
 
   long long sum = 0;
   for (int b = b0; b < b1; ++b) {
     const int c = context_lens[b];
     if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
-    sum += clamp_ctx(c, ctx_cap);
-    if (clamp_ctx(c, ctx_cap) == 0)  // an empty context attends to nothing: zeros
+    const int cc = clamp_ctx(c, ctx_cap), st = start_of(b);
+    if (cc < st) flag_status(status, PA_STATUS_BAD_CONTEXT);
+    sum += max(0, cc - st);
+    if (cc == 0 && reserved_of(b) == 0)  // an empty context attends to nothing: zeros
       for (int i = 0; i < out_row_vec16; ++i) out[(size_t)b * out_row_vec16 + i] = make_int4(0, 0, 0, 0);
   }
 #pragma unroll
@@ -107,12 +129,13 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
+  auto suffix_of = [&](int b) { return max(0, clamp_ctx(context_lens[b], ctx_cap) - start_of(b)); };
 
   int local = 0;
   for (int b = b0; b < b1; ++b) {
-    const int c = clamp_ctx(context_lens[b], ctx_cap);
+    const int c = suffix_of(b);
     const int np = (c + psz - 1) / psz;
-    local += np;
+    local += np + reserved_of(b);
     if (np > 0) {
       const int tail = c - (np - 1) * psz;
       atomicAdd(&s_hist[(tail + block_size - 1) / block_size], 1);
@@ -142,7 +165,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   int run = s_off[wid] + incl - local;
   for (int b = b0; b < b1; ++b) {
     ws.part_start[b] = run;
-    run += (clamp_ctx(context_lens[b], ctx_cap) + psz - 1) / psz;
+    run += (suffix_of(b) + psz - 1) / psz + reserved_of(b);
   }
   if (tid == 0) ws.part_start[num_seqs] = s_total;
   if (wid == 0) {
@@ -169,30 +192,31 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
       if (bucket >= 1) s_hist[bucket] = off;
       off += v[k];
     }
+    if (lane == 31) s_units = incl;  // partitions with a K/V range of their own
   }
   __syncthreads();
   run = s_off[wid] + incl - local;
   for (int b = b0; b < b1; ++b) {
-    const int c = clamp_ctx(context_lens[b], ctx_cap);
+    const int c = suffix_of(b), st = start_of(b), rs = reserved_of(b);
     const int np = (c + psz - 1) / psz;
     for (int p = 0; p < np; ++p) {
       const int ntok = min(psz, c - p * psz);
       const int slot = atomicAdd(&s_hist[(ntok + block_size - 1) / block_size], 1);
       PartRec r;
       r.b = b;
-      r.p = p;
-      r.tok0 = p * psz;
+      r.p = rs + p;
+      r.tok0 = st + p * psz;
       r.ntok = ntok;
       r.part_start = run;
-      r.nparts = np;
+      r.nparts = np + rs;
       r.pad0 = r.pad1 = 0;
       ws.parts[slot] = r;
     }
-    run += np;
+    run += np + rs;
   }
   if (tid == 0) {
     ws.header[0] = 0;
-    ws.header[1] = s_total * num_kv_heads;
+    ws.header[1] = s_units * num_kv_heads;
     ws.header[2] = psz;
     ws.header[3] = s_total;
   }
@@ -295,7 +319,9 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p,
   const int b = w / p.num_q_heads, hq = w - b * p.num_q_heads;
   const int ps = p.ws.part_start[b];
   const int np = p.ws.part_start[b + 1] - ps;
-  if (np <= 1) return;  // written by the attention kernel (or zeroed by the plan)
+  // one partition: written by the attention kernel (or zeroed by the plan), unless the
+  // sequence reads a shared prefix, whose partials always go through the merge
+  if (np <= 1 && !(p.ws.seq_flags != nullptr && p.ws.seq_flags[b])) return;
   if (head_dim == 128) {
     if (p.out_bytes == 4) merge_row<128, float>(p, b, hq, ps, np, static_cast<float*>(p.out), lane);
     else if (p.out_bf16) merge_row<128, __nv_bfloat16>(p, b, hq, ps, np, static_cast<__nv_bfloat16*>(p.out), lane);
@@ -813,39 +839,65 @@ size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_s
 
 namespace {
 struct WsLayout {
-  size_t header, part_start, units, part_ml, part_acc, total;
+  size_t header, part_start, seq_flags, units, part_ml, part_acc, total;
 };
 WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
-                       int block_size) {
+                       int block_size, long long extra_slots) {
   const size_t parts = decode_max_parts(num_seqs, num_kv_heads, max_ctx, block_size);
+  const size_t slots = parts + (size_t)extra_slots;
   WsLayout l;
   l.header = 0;
   l.part_start = 256;
-  l.units = align_up(l.part_start + sizeof(int) * (num_seqs + 1), 256);
+  l.seq_flags = align_up(l.part_start + sizeof(int) * (num_seqs + 1), 256);
+  l.units = align_up(l.seq_flags + (extra_slots > 0 ? sizeof(int) * num_seqs : 0), 256);
   l.part_ml = align_up(l.units + sizeof(PartRec) * parts, 256);
-  l.part_acc = align_up(l.part_ml + sizeof(float2) * parts * num_q_heads, 256);
-  l.total = align_up(l.part_acc + sizeof(float) * parts * num_q_heads * head_dim, 256);
+  l.part_acc = align_up(l.part_ml + sizeof(float2) * slots * num_q_heads, 256);
+  l.total = align_up(l.part_acc + sizeof(float) * slots * num_q_heads * head_dim, 256);
   return l;
 }
 }  // namespace
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int max_ctx, int block_size) {
-  return decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size).total;
+                              int max_ctx, int block_size, long long extra_slots) {
+  return decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size,
+                       extra_slots)
+      .total;
 }
 
 DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads, int num_kv_heads,
-                                       int head_dim, int max_ctx, int block_size) {
-  const WsLayout l =
-      decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size);
+                                       int head_dim, int max_ctx, int block_size,
+                                       long long extra_slots) {
+  const WsLayout l = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                   block_size, extra_slots);
   uint8_t* b = static_cast<uint8_t*>(ws);
   DecodeWorkspace w;
   w.header = reinterpret_cast<int*>(b + l.header);
   w.part_start = reinterpret_cast<int*>(b + l.part_start);
+  w.seq_flags = extra_slots > 0 ? reinterpret_cast<int*>(b + l.seq_flags) : nullptr;
   w.parts = reinterpret_cast<PartRec*>(b + l.units);
   w.part_ml = reinterpret_cast<float2*>(b + l.part_ml);
   w.part_acc = reinterpret_cast<float*>(b + l.part_acc);
   return w;
+}
+
+PrefixPlan plan_prefix(int num_sharers, int prefix_len, int group, int num_kv_heads) {
+  PrefixPlan pp = {};
+  pp.num_sharers = num_sharers;
+  pp.prefix_len = prefix_len;
+  if (num_sharers <= 0 || prefix_len <= 0) {
+    pp.num_sharers = 0;
+    pp.splits = 0;
+    return pp;
+  }
+  constexpr int kTile = 128, kRowsPerCta = 256, kTargetCtas = 152;  // one wave
+  const long long row_ctas = ((long long)num_sharers * group + kRowsPerCta - 1) / kRowsPerCta;
+  const long long tiles = (prefix_len + kTile - 1) / kTile;
+  long long want = (kTargetCtas + row_ctas * num_kv_heads - 1) / (row_ctas * num_kv_heads);
+  want = std::max(1ll, std::min(want, tiles));
+  const long long split_tiles = (tiles + want - 1) / want;
+  pp.split_tokens = (int)(split_tiles * kTile);
+  pp.splits = (int)((prefix_len + pp.split_tokens - 1) / pp.split_tokens);
+  return pp;
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -857,8 +909,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
   cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
-                             static_cast<int4*>(a.out), out_row_vec16);
+                             static_cast<int4*>(a.out), out_row_vec16, a.prefix);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
+  if (a.prefix.num_sharers > 0) {
+    const int rc = launch_shared_prefix(a, stream);
+    if (rc != PA_OK) return rc;
+  }
   DecodeParams p;
   p.q = a.q;
   p.out = a.out;

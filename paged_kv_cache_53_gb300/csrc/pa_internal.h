@@ -90,17 +90,30 @@ struct PartRec {
 struct DecodeWorkspace {
   int* header;        // [0] unit counter, [1] units, [2] part_tokens, [3] partitions
   int* part_start;    // [num_seqs + 1] first partition index of each sequence
+  int* seq_flags;     // [num_seqs] 1 for a sequence reading the shared prefix (or null)
   PartRec* parts;     // [max_parts] partitions, largest first
   float2* part_ml;    // [max_parts * num_q_heads] (running max in log2 units, sum)
   float* part_acc;    // [max_parts * num_q_heads * head_dim] unnormalised outputs
 };
 
+// A prefix of `prefix_len` tokens held once and read by every sequence listed in
+// `sharers`: its attention is computed once per KV head for all of them, in `splits`
+// pieces of `split_tokens` tokens, into partial slots the plan reserves ahead of each
+// sharer's own partitions.  num_sharers = 0 for a plain decode.
+struct PrefixPlan {
+  const int32_t* sharers;
+  const int32_t* prefix_blocks;
+  int num_sharers, prefix_len, splits, split_tokens;
+};
+
 size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int max_ctx, int block_size);
+                              int max_ctx, int block_size, long long extra_slots = 0);
 DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads,
                                        int num_kv_heads, int head_dim, int max_ctx,
-                                       int block_size);
+                                       int block_size, long long extra_slots = 0);
+// Splits of a shared prefix: about two CTAs per SM of work, in whole 128-token tiles.
+PrefixPlan plan_prefix(int num_sharers, int prefix_len, int group, int num_kv_heads);
 
 struct DecodeArgs {
   void* out;
@@ -117,7 +130,12 @@ struct DecodeArgs {
   pa_dtype dtype;
   DecodeWorkspace ws;
   int32_t* status;
+  PrefixPlan prefix;  // num_sharers = 0: no shared prefix
 };
+
+// Attention of a shared prefix for all of its sharers (pa_shared_prefix.cu): writes
+// their prefix partials into the slots the decode plan reserved.
+int launch_shared_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 // Launches the plan, attention and merge kernels.  Returns PA_OK or a PA_ERR_* code (after
 // recording the reason).

@@ -1,0 +1,440 @@
+// Attention of one shared prefix for every sequence that reads it, on sm_103a tensor
+// cores (tcgen05).
+//
+// When many sequences point their tables at the same physical prefix blocks ("Continuous
+// batching, paged attention, prefix caching", section "Prefix caching"), their decode
+// queries all attend to the same prefix K/V.  Per KV head h, the query groups of all the
+// sharers form the rows of one dense product with the prefix's K/V, so the prefix is read
+// once instead of once per sequence.  This kernel computes, for each sharer and each
+// piece ("split") of the prefix, the partial (running max, sum, unnormalised output) in
+// the same form as the decode kernels' split-KV partials, into slots the decode plan
+// reserved ahead of the sharer's own partitions; the decode merge then combines them.
+//
+// CTA (pair, split, h) owns two 128-row query tiles; row r of the pair is sharer
+// (pair * 256 + r) / G, query head h * G + r % G.  The pipeline is the chunked-prefill
+// kernel's: a TMA producer warp streams 128-token K/V tiles of the prefix through the
+// prefix's block list into a ring; one thread issues S = Q K^T and O += P V (P as hi +
+// lo 16-bit terms written into S's TMEM columns); two softmax warpgroups, one per query
+// tile, run the online softmax.  The query rows are gathered from scattered sequences,
+// so every thread of the CTA copies a share of them into 128-byte-swizzled shared memory
+// before the pipeline starts.  No causal mask: every row sees the whole split.
+#include <algorithm>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_launch.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int D, int BS>
+struct SpCfg {
+  static constexpr int BM = 128, kTiles = 2, BN = 128;
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQHalfBytes = BM * 128;
+  static constexpr int kQBytes = kHalves * kQHalfBytes;
+  static constexpr int kKvHalfBytes = BN * 128;
+  static constexpr int kKBytes = kHalves * kKvHalfBytes;
+  static constexpr int kStageBytes = 2 * kKBytes;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kBlocksPerTile = BN / BS;
+  static constexpr int kThreads = 384;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kBars = 2 * kStages + 3 * kTiles;
+  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
+                                  kBars * 8 + 16;
+};
+
+template <typename T>
+struct SpFmt;
+template <>
+struct SpFmt<__half> {
+  static constexpr int v = 0;
+};
+template <>
+struct SpFmt<__nv_bfloat16> {
+  static constexpr int v = 1;
+};
+
+struct SpParams {
+  const void* q;
+  const int32_t* sharers;
+  const int32_t* prefix_blocks;
+  const int* part_start;
+  float2* part_ml;
+  float* part_acc;
+  int32_t* status;
+  int num_sharers, prefix_len, split_tokens;
+  int num_q_heads, num_kv_heads, group, num_blocks;
+  float scale_log2;
+};
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(384, 1)
+    shared_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv, const SpParams p) {
+  using C = SpCfg<D, BS>;
+  constexpr int BN = C::BN, S = C::kStages, NT = C::kTiles;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sKV = sQ + NT * C::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + S;
+  uint64_t* s_full = bars + 2 * S;
+  uint64_t* p_full = s_full + NT;
+  uint64_t* pv_done = p_full + NT;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x, split = blockIdx.y, h = blockIdx.z;
+  const int G = p.group;
+  const int rows_total = p.num_sharers * G;
+  const int row0 = pair * NT * C::BM;
+  const int kv_begin = split * p.split_tokens;
+  const int kv_end = min(p.prefix_len, kv_begin + p.split_tokens);
+  const int n_kv = (kv_end - kv_begin + BN - 1) / BN;
+  const int nblk = p.prefix_len / BS;
+
+  griddep_wait();  // the decode plan's partial slots (part_start) are written
+
+  // the query rows of both tiles, gathered from their sequences (rows past the sharers
+  // read zeros)
+  for (int idx = threadIdx.x; idx < NT * C::BM * (D / 8); idx += blockDim.x) {
+    const int rr = idx / (D / 8), c = idx - rr * (D / 8);
+    const int x = rr / C::BM, r = rr - x * C::BM;
+    const int grow = row0 + rr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (grow < rows_total) {
+      const int i = grow / G, g = grow - i * G;
+      const int sb = __ldg(p.sharers + i);
+      v = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                               ((size_t)sb * p.num_q_heads + h * G + g) * D) +
+                c);
+    }
+    *reinterpret_cast<uint4*>(sQ + x * C::kQBytes + (c >> 3) * C::kQHalfBytes + r * 128 +
+                              (((c & 7) ^ (r & 7)) << 4)) = v;
+  }
+  tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_addr(kv_full + i), 1);
+      mbar_init(smem_addr(kv_empty + i), 1);
+    }
+    for (int x = 0; x < NT; ++x) {
+      mbar_init(smem_addr(s_full + x), 1);
+      mbar_init(smem_addr(p_full + x), 128);
+      mbar_init(smem_addr(pv_done + x), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x == 33) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool valid[NT];
+#pragma unroll
+  for (int x = 0; x < NT; ++x) valid[x] = row0 + x * C::BM < rows_total;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    const uint64_t keep = l2_policy_evict_last();  // the prefix is re-read by other CTAs
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int s = j % S;
+      if (!mbar_wait(smem_addr(kv_empty + s), ((j / S) & 1) ^ 1)) { ok = false; break; }
+      const int bi = (kv_begin + j * BN) / BS + lane;
+      int id = -1;
+      if (lane < C::kBlocksPerTile && bi < nblk && bi * BS < kv_end) {
+        id = __ldg(p.prefix_blocks + bi);
+        if (id < 0 || id >= p.num_blocks) {
+          flag_status(p.status, PA_STATUS_BAD_BLOCK);
+          id = -1;
+        }
+      }
+      uint8_t* st = sKV + s * C::kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(smem_addr(kv_full + s), C::kStageBytes);
+#pragma unroll
+      for (int i = 0; i < C::kBlocksPerTile; ++i) {
+        const int idi = __shfl_sync(~0u, id, i);
+        if (lane == 0) {
+          const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
+#pragma unroll
+          for (int hb = 0; hb < C::kHalves; ++hb) {
+            const int off = hb * C::kKvHalfBytes + i * BS * 128;
+            tma_load_2d(smem_addr(st + off), &tmk, hb * 64, y, smem_addr(kv_full + s), keep);
+            tma_load_2d(smem_addr(st + C::kKBytes + off), &tmv, hb * 64, y,
+                        smem_addr(kv_full + s), keep);
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    // PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... as in the chunked-prefill kernel
+    if (lane == 0) {
+      const uint32_t id_s = tc::idesc_f16(SpFmt<T>::v, C::BM, BN, false, false);
+      const uint32_t id_o = tc::idesc_f16(SpFmt<T>::v, C::BM, D, false, true);
+      auto issue_s = [&](int x, int j) {
+        const uint32_t tS = tmem + x * BN;
+        const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
+        const uint32_t sk = smem_addr(sKV + (j % S) * C::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t a = tc::smem_desc_sw128(sq + (kk >> 2) * C::kQHalfBytes + koff, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(sk + (kk >> 2) * C::kKvHalfBytes + koff, 16, 1024);
+          tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
+        }
+        tc::commit(smem_addr(s_full + x));
+      };
+      auto issue_pv = [&](int x, int j) -> bool {
+        if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t tP = tmem + x * BN;
+        const uint32_t tO = tmem + NT * BN + x * D;
+        const uint32_t sv = smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
+          const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
+          tc::mma_f16_ts(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
+          tc::mma_f16_ts(tO, tP + col + 16, bdesc, id_o, true);
+        }
+        tc::commit(smem_addr(pv_done + x));
+        return true;
+      };
+      if (!mbar_wait(smem_addr(kv_full), 0)) ok = false;
+      if (ok) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int x = 0; x < NT; ++x)
+          if (valid[x]) issue_s(x, 0);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        bool next_ready = false;
+#pragma unroll
+        for (int x = 0; x < NT; ++x) {
+          if (!valid[x]) continue;
+          if (!issue_pv(x, j)) { ok = false; break; }
+          if (j + 1 < n_kv) {
+            if (!next_ready) {
+              if (!mbar_wait(smem_addr(kv_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
+              tc::fence_after_sync();
+              next_ready = true;
+            }
+            issue_s(x, j + 1);
+          }
+        }
+        tc::commit(smem_addr(kv_empty + j % S));
+      }
+      if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------- softmax / partial output (one WG per tile) -------------------------
+    const int x = (warp - 4) >> 2;
+    const int r = (threadIdx.x - 128) & 127;
+    const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + x * BN;
+    const uint32_t tO = tmem + lane_bits + NT * BN + x * D;
+    const bool tile_valid = x == 0 ? valid[0] : valid[NT - 1];
+    const float sc = p.scale_log2;
+    float m = kNegInf, l = 0.f;
+    for (int j = 0; j < n_kv && tile_valid; ++j) {
+      if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      const int kp0 = kv_begin + j * BN;
+      const bool full = kp0 + BN <= kv_end;
+      float mx = kNegInf;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        float a[32], bq[32];
+        tc::tmem_ld32(tS + c0, a);
+        tc::tmem_ld32(tS + c0 + 32, bq);
+        tc::tmem_wait_ld();
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(a[i] * sc, bq[i] * sc));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            mx = fmaxf(mx, kp0 + c0 + i < kv_end ? a[i] * sc : kNegInf);
+            mx = fmaxf(mx, kp0 + c0 + 32 + i < kv_end ? bq[i] * sc : kNegInf);
+          }
+        }
+      }
+      const bool need = mx > m + kRescaleThreshold;
+      const float alpha = need ? fast_exp2(m - mx) : 1.f;
+      if (need) m = mx;
+      float sum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float a[32];
+        tc::tmem_ld32(tS + c0, a);
+        tc::tmem_wait_ld();
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sum += a[2 * i] + a[2 * i + 1];
+          hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+        }
+        tc::tmem_st16(tS + c0, hi);
+        tc::tmem_st16(tS + c0 + 16, lo);
+      }
+      l = l * alpha + sum;
+      if (j >= 1 && __any_sync(~0u, need)) {
+        if (!mbar_wait(smem_addr(pv_done + x), (j - 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tc::tmem_ld32(tO + c0, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tc::tmem_st32(tO + c0, o);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(smem_addr(p_full + x));
+    }
+    // the partial of each row: (m, l) and the unnormalised O, into the sharer's slot
+    if (ok && tile_valid && n_kv > 0 && mbar_wait(smem_addr(pv_done + x), (n_kv - 1) & 1)) {
+      tc::fence_after_sync();
+      const int grow = row0 + x * C::BM + r;
+      const bool row_ok = grow < rows_total;
+      size_t slot = 0;
+      int hq = 0;
+      if (row_ok) {
+        const int i = grow / G, g = grow - i * G;
+        const int sb = __ldg(p.sharers + i);
+        slot = (size_t)(p.part_start[sb] + split) * p.num_q_heads;
+        hq = h * G + g;
+        p.part_ml[slot + hq] = make_float2(m, l);
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        tc::tmem_ld32(tO + c0, o);
+        tc::tmem_wait_ld();
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + (slot + hq) * D + c0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+      }
+    } else if (!ok) {
+      flag_status(p.status, PA_STATUS_TIMEOUT);
+    }
+  }
+  griddep_launch_dependents();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+constexpr int kMaxDev = 64;
+std::mutex g_mutex;
+
+template <typename T, int D, int BS>
+int launch_t(const DecodeArgs& a, cudaStream_t stream) {
+  using C = SpCfg<D, BS>;
+  static bool configured[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDev)
+    return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: no usable device");
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(shared_prefix_kernel<T, D, BS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)C::kSmem) != cudaSuccess)
+        return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: shared-memory configuration failed");
+      configured[dev] = true;
+    }
+  }
+  CUtensorMap tmk, tmv;
+  const int r1 = encode_cache_map(&tmk, a.k_cache, a.dtype, a.num_blocks, a.num_kv_heads,
+                                  a.block_size, a.head_dim);
+  const int r2 = encode_cache_map(&tmv, a.v_cache, a.dtype, a.num_blocks, a.num_kv_heads,
+                                  a.block_size, a.head_dim);
+  if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS)
+    return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: cuTensorMapEncodeTiled failed");
+  SpParams p;
+  p.q = a.q;
+  p.sharers = a.prefix.sharers;
+  p.prefix_blocks = a.prefix.prefix_blocks;
+  p.part_start = a.ws.part_start;
+  p.part_ml = a.ws.part_ml;
+  p.part_acc = a.ws.part_acc;
+  p.status = a.status;
+  p.num_sharers = a.prefix.num_sharers;
+  p.prefix_len = a.prefix.prefix_len;
+  p.split_tokens = a.prefix.split_tokens;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale * kLog2e;
+  const long long rows = (long long)a.prefix.num_sharers * p.group;
+  const long long pairs = (rows + C::BM * C::kTiles - 1) / (C::BM * C::kTiles);
+  if (pairs > 0x7fffffffll || a.prefix.splits > 65535 || a.num_kv_heads > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: grid too large");
+  const cudaError_t e =
+      launch_pdl(shared_prefix_kernel<T, D, BS>,
+                 dim3((unsigned)pairs, a.prefix.splits, a.num_kv_heads), dim3(C::kThreads),
+                 C::kSmem, stream, tmk, tmv, p);
+  if (e != cudaSuccess)
+    return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+template <typename T>
+int dispatch(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.head_dim == 128 && a.block_size == 16) return launch_t<T, 128, 16>(a, stream);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_t<T, 128, 32>(a, stream);
+  if (a.head_dim == 64 && a.block_size == 16) return launch_t<T, 64, 16>(a, stream);
+  if (a.head_dim == 64 && a.block_size == 32) return launch_t<T, 64, 32>(a, stream);
+  return fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: head_dim %d / block_size %d",
+              a.head_dim, a.block_size);
+}
+
+}  // namespace
+
+int launch_shared_prefix(const DecodeArgs& a, cudaStream_t stream) {
+  return a.dtype == PA_BF16 ? dispatch<__nv_bfloat16>(a, stream) : dispatch<__half>(a, stream);
+}
+
+}  // namespace pa

@@ -62,7 +62,8 @@ class StepRun:
                 if k not in ("k_cache", "v_cache")}
 
     # ------------------------------------------------------------------ library calls
-    def run(self, out_dtype: Optional[torch.dtype] = torch.float32, kinds=("decode", "prefill")):
+    def run(self, out_dtype: Optional[torch.dtype] = torch.float32, kinds=("decode", "prefill"),
+            share_prefix: bool = False):
         import paged_kv_cache_53_gb300 as pa
         st, sh = self.step, self.step.shape
         kc, vc = self.vals["k_cache"], self.vals["v_cache"]
@@ -81,12 +82,23 @@ class StepRun:
             od = out_dtype or kc.dtype
             out = torch.empty((b.num_seqs, sh.num_q_heads, sh.head_dim), dtype=od,
                               device=self.device)
-            ws = torch.empty(pa.decode_workspace_bytes(b.num_seqs, sh.num_q_heads,
-                                                       sh.num_kv_heads, sh.head_dim, b.max_ctx,
-                                                       sh.block_size),
-                             dtype=torch.uint8, device=self.device)
-            pa.decode(out, self.vals["q_decode"], kc, vc, m["bt"], m["ctx"], b.max_ctx, st.scale,
-                      ws)
+            if share_prefix:
+                blocks, plen, sharers = st.shared_prefix
+                nbytes = pa.decode_shared_prefix_workspace_bytes(
+                    b.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, b.max_ctx,
+                    sh.block_size, len(sharers), plen)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+                pa.decode_shared_prefix(out, self.vals["q_decode"], kc, vc, m["bt"], m["ctx"],
+                                        b.max_ctx, torch.from_numpy(blocks).to(self.device),
+                                        plen, torch.from_numpy(sharers).to(self.device),
+                                        st.scale, ws)
+            else:
+                ws = torch.empty(pa.decode_workspace_bytes(b.num_seqs, sh.num_q_heads,
+                                                           sh.num_kv_heads, sh.head_dim,
+                                                           b.max_ctx, sh.block_size),
+                                 dtype=torch.uint8, device=self.device)
+                pa.decode(out, self.vals["q_decode"], kc, vc, m["bt"], m["ctx"], b.max_ctx,
+                          st.scale, ws)
             res["out_decode"] = out
         if "prefill" in self.meta and "prefill" in kinds:
             b, m = st.prefill, self.meta["prefill"]

@@ -113,3 +113,40 @@ def test_cache_ops_reject_bad_arguments(lib):
 
 def test_get_status_without_output_pointer(lib):
     assert lib.pa_get_status(None) == 1
+
+
+def _shared(lib, **kw):
+    a = dict(out=FAKE, out_dtype=2, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxblk=64, ctx=FAKE,
+             max_ctx=1024, B=4, Hq=32, Hkv=8, D=128, BS=16, NB=64, pb=FAKE, plen=512, sh=FAKE,
+             nsh=3, scale=0.1, dt=2, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.pa_decode_shared_prefix(
+        a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["bt"], a["maxblk"], a["ctx"],
+        a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["BS"], a["NB"], a["pb"], a["plen"],
+        a["sh"], a["nsh"], a["scale"], a["dt"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(plen=500), 1, "multiple of the block size"),
+    (dict(plen=2048), 1, "max_ctx"),
+    (dict(dt=0, out_dtype=0), 2, "fp16/bf16"),
+    (dict(sh=None), 1, "null"),
+    (dict(pb=None), 1, "null"),
+    (dict(nsh=-1), 1, "negative"),
+    (dict(ws_bytes=1 << 20), 3, "workspace"),
+    (dict(D=96), 2, "head_dim"),
+])
+def test_shared_prefix_rejects_bad_arguments(lib, kw, code, needle):
+    assert _shared(lib, **kw) == code
+    assert needle in _err(lib)
+
+
+def test_shared_prefix_workspace_bytes(lib):
+    f = lib.pa_decode_shared_prefix_workspace_bytes
+    plain = lib.pa_decode_workspace_bytes(160, 32, 8, 128, 2560, 16)
+    assert f(160, 32, 8, 128, 2560, 16, 0, 2048) == plain  # no sharers: the plain layout
+    assert f(160, 32, 8, 128, 2560, 16, 128, 0) == plain
+    with_prefix = f(160, 32, 8, 128, 2560, 16, 128, 2048)
+    # every sharer keeps one fp32 partial row per query head and prefix split
+    assert with_prefix >= plain + 128 * 32 * 128 * 4
+    assert f(160, 30, 8, 128, 2560, 16, 128, 2048) == 0

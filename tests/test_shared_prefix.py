@@ -1,0 +1,157 @@
+"""Decode with a shared prefix attended once (pa_decode_shared_prefix) against the float64
+oracle, which walks every sequence's full block table on its own.
+
+Bar: the decode bar, max |gpu - oracle| <= 2e-3 on fp32 outputs for fp16/bf16 inputs;
+cache writes and copies of the same steps bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from pa_harness import TOL, StepRun, half_ulp, oracle_step, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_cache_53_gb300 as pa
+    pa.get_status()
+    return pa
+
+
+def _check(pa, step, out_dtype=torch.float32):
+    run = StepRun(step)
+    kc, vc = run.host_pool()
+    vals = run.host_values()
+    res = run.run(out_dtype=out_dtype, share_prefix=True)
+    ref = oracle_step(step, kc, vc, vals)
+    assert np.array_equal(W.to_numpy(run.vals["k_cache"]), kc)
+    assert np.array_equal(W.to_numpy(run.vals["v_cache"]), vc)
+    got = to_f64(res["out_decode"])
+    err = np.abs(got - ref["out_decode"])
+    tol = TOL[step.shape.dtype]
+    if out_dtype != torch.float32:
+        tol = tol + half_ulp(ref["out_decode"], step.shape.dtype)
+    assert np.all(err <= tol), f"max err {err.max():.3g} at {np.unravel_index(err.argmax(), err.shape)}"
+    assert pa.get_status() == 0
+    return run, res
+
+
+def test_prefix_sharing_cow_workload(pa):
+    """The prefix-sharing workload (128 rows on one 2048-token prefix, 8 groups of 4
+    samples with copy-on-write) through the shared-prefix entry point."""
+    _check(pa, W.prefix_sharing_cow())
+
+
+def test_matches_plain_decode(pa):
+    """Same inputs through pa_decode and pa_decode_shared_prefix: both within the bar, and
+    close to each other (they differ only in summation order)."""
+    step = W.prefix_sharing_cow()
+    a = StepRun(step).run(kinds=("decode",))["out_decode"]
+    b = StepRun(step).run(kinds=("decode",), share_prefix=True)["out_decode"]
+    assert torch.max(torch.abs(a - b)).item() <= 2e-3
+    assert pa.get_status() == 0
+
+
+# ------------------------------------------------------------------ shapes and edges
+def _suffixes(n, seed, hi=300, with_zero=True):
+    rng = np.random.default_rng(seed)
+    s = rng.integers(1, hi, size=n, endpoint=True)
+    if with_zero and n > 1:
+        s[n // 2] = 0  # one row whose context ends at the prefix
+    return s
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d,bs", [(128, 16), (128, 32), (64, 16), (64, 32)])
+@pytest.mark.parametrize("h_q,h_kv", [(32, 8), (8, 8), (16, 2)])
+def test_shapes(pa, dtype, d, bs, h_q, h_kv):
+    # 592 = 37 blocks of 16 (not a whole number of 128-token tiles); 576 for block 32
+    prefix = 592 if bs == 16 else 576
+    step = W.shared_prefix_step("sp", W.Shape(h_q, h_kv, d, bs, dtype), prefix,
+                                _suffixes(37, 11), [5, 700, 1], seed=12)
+    _check(pa, step)
+
+
+@pytest.mark.parametrize("n_sharers", [1, 2, 63, 64, 65, 200])
+def test_sharer_counts(pa, n_sharers):
+    """Ragged query-row tiles: G = 4 rows per sharer, 256 rows per CTA."""
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 1024,
+                                _suffixes(n_sharers, n_sharers), [33, 2000], seed=n_sharers)
+    _check(pa, step)
+
+
+@pytest.mark.parametrize("prefix", [16, 128, 144, 4096, 8192])
+def test_prefix_lengths(pa, prefix):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), prefix,
+                                _suffixes(24, prefix), [prefix + 17], seed=prefix)
+    _check(pa, step)
+
+
+def test_only_sharers_ending_at_the_prefix(pa):
+    """A sharer with no context of its own gets the prefix's attention alone (the merge
+    normalises its single partial)."""
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [0], [], seed=4)
+    _check(pa, step)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_native_output(pa, dtype):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, dtype), 512, _suffixes(50, 3),
+                                [100], seed=5)
+    _check(pa, step, out_dtype=getattr(torch, {"bf16": "bfloat16", "f16": "float16"}[dtype]))
+
+
+def test_no_sharers_is_plain_decode_bit_for_bit(pa):
+    """num_sharers = 0 runs pa_decode's kernels unchanged."""
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 512, _suffixes(20, 6),
+                                [300, 9], seed=6)
+    step = W.replace(step, shared_prefix=(step.shared_prefix[0], 512, np.zeros(0, np.int32)))
+    a = StepRun(step).run(kinds=("decode",))["out_decode"]
+    b = StepRun(step).run(kinds=("decode",), share_prefix=True)["out_decode"]
+    assert torch.equal(a, b)
+    assert pa.get_status() == 0
+
+
+def test_is_deterministic(pa):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 2048, _suffixes(96, 8),
+                                [512], seed=8)
+    a = StepRun(step).run(kinds=("decode",), share_prefix=True)["out_decode"]
+    b = StepRun(step).run(kinds=("decode",), share_prefix=True)["out_decode"]
+    assert torch.equal(a, b)
+
+
+def test_bad_prefix_block_is_flagged(pa):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [4, 9], [], seed=9)
+    run = StepRun(step)
+    blocks, plen, sharers = step.shared_prefix
+    bad = blocks.copy()
+    bad[3] = step.num_blocks + 5
+    run.step = W.replace(step, shared_prefix=(bad, plen, sharers))
+    run.run(kinds=("decode",), share_prefix=True)
+    assert pa.get_status() & pa.STATUS_BAD_BLOCK
+
+
+def test_sharer_shorter_than_the_prefix_is_flagged(pa):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [4, 9], [40],
+                                seed=10)
+    blocks, plen, _ = step.shared_prefix
+    run = StepRun(W.replace(step, shared_prefix=(blocks, plen, np.array([0, 2], np.int32))))
+    run.run(kinds=("decode",), share_prefix=True)
+    assert pa.get_status() & pa.STATUS_BAD_CONTEXT
+
+
+def test_rejects_bad_arguments(pa):
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [4, 9], [], seed=1)
+    run = StepRun(step)
+    blocks, plen, sharers = step.shared_prefix
+    for bad in [(blocks, 250, sharers), (blocks, 4096, sharers)]:
+        run.step = W.replace(step, shared_prefix=bad)
+        with pytest.raises(pa.PaError):
+            run.run(kinds=("decode",), share_prefix=True)
+    step32 = W.shared_prefix_step("sp", W.Shape(8, 8, 64, 16, "f32"), 64, [4], [], seed=1)
+    with pytest.raises(pa.PaError):
+        StepRun(step32).run(kinds=("decode",), share_prefix=True)
+    pa.get_status()

@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import dataclasses
 from dataclasses import dataclass
-from typing import Dict, Optional
+from typing import Dict, Optional, Tuple
 
 import numpy as np
 
@@ -111,6 +111,9 @@ class Step:
     prefill: Optional[Batch] = None
     cow_pairs: Optional[np.ndarray] = None  # int32 [N, 2] (src, dst)
     decode_tables_before_cow: Optional[np.ndarray] = None
+    # one physical prefix read by several decode sequences: (prefix blocks int32,
+    # prefix length in tokens, indices of the decode rows that start with it)
+    shared_prefix: Optional[Tuple[np.ndarray, int, np.ndarray]] = None
     notes: str = ""
 
     def batches(self):
@@ -153,6 +156,41 @@ def decode_step(name: str, shape: Shape, context_lens, seed: int, *,
     return Step(name=name, shape=shape, num_blocks=nb, seed=seed,
                 scale=scale if scale is not None else 1.0 / np.sqrt(shape.head_dim),
                 decode=batch)
+
+
+def shared_prefix_step(name: str, shape: Shape, prefix_len: int, suffix_lens, other_ctx,
+                       seed: int, *, headroom: float = 0.10) -> Step:
+    """A decode step in which rows 0 .. len(suffix_lens)-1 start with one shared
+    `prefix_len`-token prefix (a whole number of blocks held once in the pool) followed by
+    suffix_lens[i] private tokens (the appended token included when > 0; a row with suffix
+    0 appends the prefix's last token itself, so at most one such row is allowed), and
+    rows after them have private contexts `other_ctx`."""
+    bs = shape.block_size
+    if prefix_len % bs:
+        raise ValueError("prefix_len must be a whole number of blocks")
+    suf = np.asarray(suffix_lens, dtype=np.int64)
+    if int((suf == 0).sum()) > 1:
+        raise ValueError("at most one sharer may end at the prefix")
+    oth = np.asarray(other_ctx, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    pb = prefix_len // bs
+    counts_suf, counts_oth = _nblocks(suf, bs), _nblocks(oth, bs)
+    used = pb + int(counts_suf.sum()) + int(counts_oth.sum())
+    nb = max(_pool_with_headroom(used, headroom), 1)
+    ids = iter(rng.permutation(nb).astype(np.int32).tolist())
+    take = lambda n: [next(ids) for _ in range(int(n))]
+    prefix = take(pb)
+    rows = [prefix + take(n) for n in counts_suf] + [take(n) for n in counts_oth]
+    ctx = np.concatenate([prefix_len + suf, oth]).astype(np.int32)
+    width = max(1, max(len(r) for r in rows))
+    t = np.full((len(rows), width), UNUSED_BLOCK, dtype=np.int32)
+    for b, r in enumerate(rows):
+        t[b, :len(r)] = r
+    batch = Batch(context_lens=ctx, query_lens=np.ones_like(ctx), block_tables=t)
+    return Step(name=name, shape=shape, num_blocks=nb, seed=seed,
+                scale=1.0 / np.sqrt(shape.head_dim), decode=batch,
+                shared_prefix=(np.asarray(prefix, dtype=np.int32), int(prefix_len),
+                               np.arange(len(suf), dtype=np.int32)))
 
 
 def prefill_step(name: str, shape: Shape, context_lens, query_lens, seed: int, *,
@@ -278,6 +316,8 @@ def prefix_sharing_cow() -> Step:
                 seed=53_003, scale=1.0 / np.sqrt(shape.head_dim), decode=batch,
                 cow_pairs=np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
                 decode_tables_before_cow=pack(rows_before),
+                shared_prefix=(np.asarray(shared_prefix, dtype=np.int32), prefix_tokens,
+                               np.arange(n_prefix_seqs, dtype=np.int32)),
                 notes="rows 0-127 share a 2048-token prefix; rows 128-159 are 8 groups of "
                       "4 samples")
 
