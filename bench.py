@@ -156,6 +156,7 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.first = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
@@ -163,6 +164,13 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+        if self.proc is not None:
+            # the timed region starts only once the sampler is up and has read the GPU
+            # once, so that its start-up does not fall inside it
+            import select
+            ready, _, _ = select.select([self.proc.stdout], [], [], 10.0)
+            if ready:
+                self.first.append(self.proc.stdout.readline())
         return self
 
     def __exit__(self, *exc):
@@ -174,6 +182,7 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
+            # the sample taken before the timed region is left out
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
@@ -389,6 +398,16 @@ def run_ours(args, rank, world, local_rank):
                        "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
                        "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV read per step "
                              "vs 0.13 GB L2"})
+        if step.shared_prefix is not None:
+            # blocks held once but read by many sequences: the metric counts every reader
+            # (logical bytes); the unique bytes are what must come from HBM at least
+            tok, _ = shared_prefix_saving(step)
+            ukv = kvb - tok * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+            config.update({
+                "unique_kv_bytes_per_step": int(ukv),
+                "value_kind": "effective (logical bytes, every reader counted; L2-assisted)",
+                "l2": f"{kvb / 1e9:.2f} GB logical, {ukv / 1e9:.3f} GB unique KV per step "
+                      "vs 0.13 GB L2"})
         res.update({
             "value": round(world * kvb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),

@@ -46,7 +46,8 @@ struct SpCfg {
   static constexpr int kBlocksPerTile = BN / BS;
   static constexpr int kThreads = 384;
   static constexpr int kTmemCols = 512;
-  static constexpr int kBars = 2 * kStages + 3 * kTiles;
+  static constexpr int kBars = 2 * kStages + 3 * kTiles + 1;
+  static constexpr int kGatherThreads = kThreads - 32;  // every warp but the producer
   static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
                                   kBars * 8 + 16;
 };
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = bars + 2 * S;
   uint64_t* p_full = s_full + NT;
   uint64_t* pv_done = p_full + NT;
+  uint64_t* q_full = pv_done + NT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = blockIdx.x, split = blockIdx.y, h = blockIdx.z;
@@ -104,27 +106,6 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = (kv_end - kv_begin + BN - 1) / BN;
   const int nblk = p.prefix_len / BS;
 
-  griddep_wait();  // the decode plan's partial slots (part_start) are written
-
-  // the query rows of both tiles, gathered from their sequences (rows past the sharers
-  // read zeros)
-  for (int idx = threadIdx.x; idx < NT * C::BM * (D / 8); idx += blockDim.x) {
-    const int rr = idx / (D / 8), c = idx - rr * (D / 8);
-    const int x = rr / C::BM, r = rr - x * C::BM;
-    const int grow = row0 + rr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (grow < rows_total) {
-      const int i = grow / G, g = grow - i * G;
-      const int sb = __ldg(p.sharers + i);
-      v = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                               ((size_t)sb * p.num_q_heads + h * G + g) * D) +
-                c);
-    }
-    *reinterpret_cast<uint4*>(sQ + x * C::kQBytes + (c >> 3) * C::kQHalfBytes + r * 128 +
-                              (((c & 7) ^ (r & 7)) << 4)) = v;
-  }
-  tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_addr(kv_full + i), 1);
@@ -135,6 +116,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(smem_addr(p_full + x), 128);
       mbar_init(smem_addr(pv_done + x), 1);
     }
+    mbar_init(smem_addr(q_full), C::kGatherThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -153,6 +135,45 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
   for (int x = 0; x < NT; ++x) valid[x] = row0 + x * C::BM < rows_total;
   bool ok = true;
+  // Only the partial slots (part_start) come from the decode plan, the kernel launched just
+  // before this one; the epilogue waits for it.  The query rows and the prefix's K/V were
+  // written before the plan started (it waits for its own predecessors before letting
+  // this kernel launch), so they are read while the plan still runs.
+
+  if (warp > 0) {
+    // the query rows of both tiles, gathered from their sequences into the 128-byte
+    // swizzled layout while the producer's first K/V tiles are in flight (rows past the
+    // sharers read zeros); kUnroll loads in flight per thread
+    constexpr int kItems = NT * C::BM * (D / 8), kUnroll = 6;
+    const int t = threadIdx.x - 32;
+    for (int i0 = t; i0 < kItems; i0 += kUnroll * C::kGatherThreads) {
+      uint4 v[kUnroll];
+      uint32_t off[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int idx = i0 + u * C::kGatherThreads;
+        const int rr = idx / (D / 8), c = idx - rr * (D / 8);
+        const int x = rr / C::BM, r = rr - x * C::BM;
+        const int grow = row0 + rr;
+        v[u] = make_uint4(0, 0, 0, 0);
+        off[u] = idx < kItems ? (uint32_t)(x * C::kQBytes + (c >> 3) * C::kQHalfBytes + r * 128 +
+                                           (((c & 7) ^ (r & 7)) << 4))
+                              : ~0u;
+        if (idx < kItems && grow < rows_total) {
+          const int si = grow / G, g = grow - si * G;
+          const int sb = __ldg(p.sharers + si);
+          v[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                      ((size_t)sb * p.num_q_heads + h * G + g) * D) +
+                       c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (off[u] != ~0u) *reinterpret_cast<uint4*>(sQ + off[u]) = v[u];
+    }
+    tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+    mbar_arrive(smem_addr(q_full));
+  }
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
         tc::commit(smem_addr(pv_done + x));
         return true;
       };
-      if (!mbar_wait(smem_addr(kv_full), 0)) ok = false;
+      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(kv_full), 0)) ok = false;
       if (ok) {
         tc::fence_after_sync();
 #pragma unroll
@@ -264,6 +285,9 @@ __global__ void __launch_bounds__(384, 1)
       tc::fence_after_sync();
       const int kp0 = kv_begin + j * BN;
       const bool full = kp0 + BN <= kv_end;
+      // row maximum; on whole tiles with a positive scale the raw scores are compared
+      // and the maximum scaled once
+      const bool raw = full && sc > 0.f;
       float mx = kNegInf;
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 64) {
@@ -271,7 +295,17 @@ __global__ void __launch_bounds__(384, 1)
         tc::tmem_ld32(tS + c0, a);
         tc::tmem_ld32(tS + c0 + 32, bq);
         tc::tmem_wait_ld();
-        if (full) {
+        if (raw) {
+          float r0 = a[0], r1 = a[1], r2 = bq[0], r3 = bq[1];
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) {
+            r0 = fmaxf(r0, a[i]);
+            r1 = fmaxf(r1, a[i + 1]);
+            r2 = fmaxf(r2, bq[i]);
+            r3 = fmaxf(r3, bq[i + 1]);
+          }
+          mx = fmaxf(mx, fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)));
+        } else if (full) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(a[i] * sc, bq[i] * sc));
         } else {
@@ -282,6 +316,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
+      if (raw) mx *= sc;
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
@@ -326,31 +361,45 @@ __global__ void __launch_bounds__(384, 1)
       tc::fence_before_sync();
       mbar_arrive(smem_addr(p_full + x));
     }
-    // the partial of each row: (m, l) and the unnormalised O, into the sharer's slot
-    if (ok && tile_valid && n_kv > 0 && mbar_wait(smem_addr(pv_done + x), (n_kv - 1) & 1)) {
+    griddep_wait();  // the decode plan's partial slots (part_start) are written
+    // the partial of each row: (m, l) and the unnormalised O, into the sharer's slot.  O
+    // goes through shared memory (this tile's query buffer, free once its last product
+    // is done) 32 columns at a time so that the global stores are whole 128-byte rows.
+    bool go = ok && tile_valid && n_kv > 0;
+    if (go && !mbar_wait(smem_addr(pv_done + x), (n_kv - 1) & 1)) ok = go = false;
+    if (__all_sync(~0u, go)) {  // warp-collective loads and shuffles below
       tc::fence_after_sync();
       const int grow = row0 + x * C::BM + r;
       const bool row_ok = grow < rows_total;
-      size_t slot = 0;
-      int hq = 0;
+      float* dst = nullptr;
       if (row_ok) {
-        const int i = grow / G, g = grow - i * G;
-        const int sb = __ldg(p.sharers + i);
-        slot = (size_t)(p.part_start[sb] + split) * p.num_q_heads;
-        hq = h * G + g;
-        p.part_ml[slot + hq] = make_float2(m, l);
+        const int si = grow / G, g = grow - si * G;
+        const int sb = __ldg(p.sharers + si);
+        const size_t row = (size_t)(p.part_start[sb] + split) * p.num_q_heads + h * G + g;
+        p.part_ml[row] = make_float2(m, l);
+        dst = p.part_acc + row * D;
       }
-#pragma unroll
+      uint8_t* stage = sQ + x * C::kQBytes + (warp & 3) * 32 * 128;  // 32 rows x 128 B
+#pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
         tc::tmem_ld32(tO + c0, o);
         tc::tmem_wait_ld();
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + (slot + hq) * D + c0);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+              make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rw = 4 * i + (lane >> 3), k = lane & 7;
+          float* d = reinterpret_cast<float*>(
+              __shfl_sync(~0u, reinterpret_cast<uintptr_t>(dst), rw));
+          const float4 v =
+              *reinterpret_cast<const float4*>(stage + rw * 128 + ((k ^ (rw & 7)) << 4));
+          if (d != nullptr) *reinterpret_cast<float4*>(d + c0 + 4 * k) = v;
         }
+        __syncwarp();
       }
     } else if (!ok) {
       flag_status(p.status, PA_STATUS_TIMEOUT);
