@@ -35,6 +35,10 @@ the functions that depend on them.
 Pins: every function here is checked in tests/test_oracle.py against numbers the pages
 print, closed forms and invariants, and against torch's CPU scaled-dot-product attention
 in float64 on contiguous tensors.
+
+`oracle.block_manager` is the reference for the host-side block manager (allocation,
+sharing with copy-on-write, prefix-cache keys with least-recently-used eviction, swap to
+host blocks), pinned in tests/test_block_manager_oracle.py.
 """
 from .paged_attention import (  # noqa: F401
     blocks_for_tokens,
