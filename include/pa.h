@@ -53,6 +53,7 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 #define PA_ERR_UNSUPPORTED 2 /* a head_dim, block_size, group size or dtype not built */
 #define PA_ERR_WORKSPACE 3   /* workspace smaller than the *_workspace_bytes() figure */
 #define PA_ERR_CUDA 4        /* the CUDA runtime refused a launch or a query */
+#define PA_ERR_NO_BLOCKS 5   /* the block manager lacks free blocks (pa_block_manager.h) */
 
 /* bits of the device status word */
 #define PA_STATUS_BAD_BLOCK 0x1   /* a block id outside [0, num_blocks) was met */

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpagedattn.so")
 SOURCES = ["pa_api.cu", "pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu",
-           "pa_decode_static.cu", "pa_shared_prefix.cu"]
+           "pa_decode_static.cu", "pa_shared_prefix.cu", "pa_block_manager.cpp",
+           "pa_sha256.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -42,7 +43,7 @@ def _flags(ptxas_info: bool):
 def _inputs():
     deps = [os.path.join(CSRC, s) for s in SOURCES]
     deps += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    deps.append(os.path.join(INCLUDE, "pa.h"))
+    deps += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     deps.append(os.path.abspath(__file__))
     return deps
 

@@ -78,6 +78,8 @@ int check_cache_geometry(const char* fn, int num_kv_heads, int head_dim, int blo
 
 }  // namespace
 
+void clear_error() { g_error[0] = '\0'; }
+
 int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

@@ -12,6 +12,8 @@ namespace pa {
 
 // Records a failure for pa_last_error_string() and returns `code`.
 int fail(int code, const char* fmt, ...);
+// Empties pa_last_error_string() at the start of an entry point.
+void clear_error();
 
 // Device address of the current device's status word (nullptr if unavailable).
 int32_t* status_word();

@@ -1,4 +1,4 @@
-"""The C-ABI library builds, loads, exports what include/pa.h declares, and rejects bad
+"""The C-ABI library builds, loads, exports what include/*.h declare, and rejects bad
 arguments on the host before anything reaches a GPU.
 
 Every call below fails validation, so no kernel is launched and no device memory is
@@ -11,7 +11,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pa.h")
+INCLUDE = os.path.join(ROOT, "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced
 
@@ -25,9 +26,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_four_operations():
