@@ -52,6 +52,7 @@ from .paged_attention import (  # noqa: F401
     prefill_chunk_attention_rows,
     reshape_and_cache,
     slot_mapping,
+    swap_blocks,
     tail_waste,
     widen,
 )

@@ -110,6 +110,16 @@ def copy_blocks(caches, pairs: np.ndarray) -> None:
             cache[dst] = cache[src]
 
 
+def swap_blocks(src_pools, dst_pools, pairs: np.ndarray) -> None:
+    """Pre-emption by swap ("Continuous batching and paged attention", section "Why they
+    depend on each other": swap to host memory instead of recomputing): for each (src,
+    dst) pair, block dst of every destination pool becomes a copy of block src of the
+    matching source pool.  Pairs are applied in order."""
+    for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
+        for s_pool, d_pool in zip(src_pools, dst_pools):
+            d_pool[dst] = s_pool[src]
+
+
 def gather_context(cache: np.ndarray, table_row: np.ndarray, ctx: int) -> np.ndarray:
     """Walks one block table row and returns the sequence's logical cache
     [ctx, num_kv_heads, head_dim]: token t comes from physical block

@@ -407,6 +407,27 @@ def test_copy_blocks_bits():
         assert np.array_equal(kc[blk], k0[blk]) and np.array_equal(vc[blk], v0[blk])
 
 
+def test_swap_blocks_round_trip_and_fancy_index():
+    """Swap-out then swap-in of the same blocks restores the pool; a swap equals numpy's
+    fancy-indexed assignment; blocks not named keep their bits."""
+    dev = [_rand((8, 2, 16, 64), "bf16", 40 + i) for i in range(4)]  # K, V of two layers
+    host = [np.zeros((5, 2, 16, 64), dtype=np.uint16) for _ in range(4)]
+    orig = [d.copy() for d in dev]
+    out = np.array([[6, 0], [1, 3], [2, 4]], dtype=np.int32)  # (device, host)
+    oracle.swap_blocks(dev, host, out)
+    for d, h in zip(orig, host):
+        ref = np.zeros_like(h)
+        ref[out[:, 1]] = d[out[:, 0]]
+        assert np.array_equal(h, ref)
+    for d in dev:  # the device blocks are reused by someone else meanwhile
+        d[[6, 1, 2]] = 0
+    back = np.array([[0, 7], [3, 1], [4, 5]], dtype=np.int32)  # (host, device)
+    oracle.swap_blocks(host, dev, back)
+    for d, o in zip(dev, orig):
+        assert np.array_equal(d[7], o[6]) and np.array_equal(d[1], o[1])
+        assert np.array_equal(d[5], o[2]) and np.array_equal(d[0], o[0])
+
+
 def test_widen_bf16_bit_patterns():
     bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0000, 0x8000, 0x7F7F], dtype=np.uint16)
     got = oracle.widen(bits, "bf16")
