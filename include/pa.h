@@ -146,6 +146,34 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                    int block_size, int num_blocks, pa_dtype dtype, void* stream);
 
 /*
+ * pa_swap_blocks -- whole-block copies between two pools, for pre-emption by swapping a
+ * sequence's blocks to host memory and back ("Continuous batching and paged attention",
+ * section "Why they depend on each other": recompute versus swap to host memory).
+ *
+ * For every pair (src, dst) and every layer, block dst of the destination K and V pools
+ * becomes a copy of block src of the source pools.  Typically one side is the device
+ * pool and the other a host pool of the same geometry in page-locked memory, which the
+ * kernel reads or writes directly through the unified address space (over the
+ * chip-to-chip link on Grace systems); device-to-device pools work as well.
+ *
+ *   src_k, src_v, dst_k, dst_v  HOST arrays of `num_layers` pool pointers (num_layers <=
+ *                   128), each [blocks, num_kv_heads, block_size, head_dim] of `dtype`,
+ *                   16-byte aligned, in this device's memory or in page-locked host
+ *                   memory (pageable memory is rejected)
+ *   pairs           int32 [num_pairs, 2] (src block, dst block), device or page-locked
+ *                   host memory; the block manager's pa_bm_swap_out / pa_bm_swap_in emit
+ *                   them
+ *   src_num_blocks, dst_num_blocks  blocks in each pool; a pair outside them is skipped
+ *                   and sets PA_STATUS_BAD_BLOCK
+ * Destinations must be distinct.  Asynchronous on `stream`; the host side must not be
+ * read (swap-out) or reused (swap-in) before the stream reaches this point.  Bit-exact.
+ */
+int pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
+                   void* const* dst_v, int num_layers, const int32_t* pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int src_num_blocks,
+                   int dst_num_blocks, pa_dtype dtype, void* stream);
+
+/*
  * pa_decode_workspace_bytes -- bytes of device workspace pa_decode needs for these
  * sizes (the split-KV partial results and the work list).  max_ctx bounds every
  * context length of the call.

@@ -21,7 +21,8 @@ from .build import LIB as LIB_PATH
 
 __all__ = [
     "PA_F32", "PA_F16", "PA_BF16", "PaError", "lib", "dtype_code",
-    "slot_mapping", "reshape_and_cache", "cache_append", "copy_blocks", "decode_workspace_bytes",
+    "slot_mapping", "reshape_and_cache", "cache_append", "copy_blocks", "swap_blocks",
+    "decode_workspace_bytes",
     "decode", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
     "prefill_workspace_bytes", "prefill_chunk", "get_status", "version",
     "STATUS_BAD_BLOCK", "STATUS_BAD_SLOT", "STATUS_BAD_CONTEXT", "STATUS_TIMEOUT",
@@ -53,6 +54,7 @@ _SIGNATURES = {
     "pa_slot_mapping": ([_p, _p, _i, _p, _p, _i, _i, _i, _i, _p], _i),
     "pa_reshape_and_cache": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _p], _i),
+    "pa_swap_blocks": ([_p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _p], _i),
     "pa_cache_append": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                          _p], _i),
     "pa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
@@ -167,6 +169,26 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     varr = (ctypes.c_void_p * n)(*[_ptr(t) for t in v_caches])
     _check(lib().pa_copy_blocks(karr, varr, n, _ptr(pairs), pairs.shape[0], h_kv, d, bs, nb,
                                 dtype_code(k_caches[0].dtype), _stream(stream)))
+
+
+def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor],
+                dst_k: Sequence[torch.Tensor], dst_v: Sequence[torch.Tensor],
+                pairs: torch.Tensor, stream=None):
+    """Block dst of every destination pool <- block src of the matching source pool, for
+    every (src, dst) row of `pairs` (see pa_swap_blocks).  Pools are CUDA tensors or
+    pinned CPU tensors of one geometry [blocks, H_kv, block_size, D]."""
+    n = len(src_k)
+    if not (n == len(src_v) == len(dst_k) == len(dst_v)) or n == 0:
+        raise ValueError("need the same non-zero number of pools on every side")
+    _i32(pairs, "pairs")
+    if pairs.device.type == "cpu" and not pairs.is_pinned():
+        raise ValueError("pairs must be a CUDA tensor or a pinned CPU tensor")
+    nbs, h_kv, bs, d = src_k[0].shape
+    nbd = dst_k[0].shape[0]
+    arr = lambda ts: (ctypes.c_void_p * n)(*[_ptr(t) for t in ts])
+    _check(lib().pa_swap_blocks(arr(src_k), arr(src_v), arr(dst_k), arr(dst_v), n, _ptr(pairs),
+                                pairs.shape[0], h_kv, d, bs, nbs, nbd,
+                                dtype_code(src_k[0].dtype), _stream(stream)))
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

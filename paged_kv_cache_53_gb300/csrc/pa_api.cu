@@ -76,6 +76,21 @@ int check_cache_geometry(const char* fn, int num_kv_heads, int head_dim, int blo
   return PA_OK;
 }
 
+// The address a kernel on the current device uses for `p`: device or managed memory of
+// this device as is, page-locked host memory through its device mapping; null for
+// pageable host memory or another device's memory.
+void* device_view(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+    return at.device == current_device() ? const_cast<void*>(p) : nullptr;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
 }  // namespace
 
 void clear_error() { g_error[0] = '\0'; }
@@ -264,6 +279,52 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                                      block_bytes, num_blocks, st,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_copy_blocks: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
+                   void* const* dst_v, int num_layers, const int32_t* pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int src_num_blocks,
+                   int dst_num_blocks, pa_dtype dtype, void* stream) {
+  g_error[0] = '\0';
+  if (num_pairs < 0 || num_layers < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: negative sizes");
+  int rc = check_cache_geometry("pa_swap_blocks", num_kv_heads, head_dim, block_size,
+                                src_num_blocks, dtype);
+  if (rc != PA_OK) return rc;
+  rc = check_cache_geometry("pa_swap_blocks", num_kv_heads, head_dim, block_size,
+                            dst_num_blocks, dtype);
+  if (rc != PA_OK) return rc;
+  if (num_pairs == 0 || num_layers == 0) return PA_OK;
+  if (num_layers > kMaxSwapLayers)
+    return fail(PA_ERR_UNSUPPORTED, "pa_swap_blocks: %d layers > %d", num_layers, kMaxSwapLayers);
+  if (!src_k || !src_v || !dst_k || !dst_v || !pairs)
+    return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: null pointer");
+  int32_t* st = status_word();
+  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_swap_blocks: no usable CUDA device");
+  void* views[4][kMaxSwapLayers];
+  void* const* in[4] = {src_k, src_v, dst_k, dst_v};
+  for (int a = 0; a < 4; ++a)
+    for (int l = 0; l < num_layers; ++l) {
+      if (!in[a][l] || !aligned16(in[a][l]))
+        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: layer %d pool pointer null or unaligned",
+                    l);
+      views[a][l] = device_view(in[a][l]);
+      if (views[a][l] == nullptr)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_swap_blocks: layer %d pool is neither this device's memory nor "
+                    "page-locked host memory",
+                    l);
+    }
+  const int32_t* pv = static_cast<const int32_t*>(device_view(pairs));
+  if (pv == nullptr || (reinterpret_cast<uintptr_t>(pairs) & 3u))
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_swap_blocks: pairs must be device or page-locked host memory, 4-byte aligned");
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * dtype_bytes(dtype);
+  cudaError_t e = launch_swap_blocks(views[0], views[1], views[2], views[3], num_layers, pv,
+                                     num_pairs, block_bytes, src_num_blocks, dst_num_blocks, st,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_swap_blocks: %s", cudaGetErrorString(e));
   return PA_OK;
 }
 

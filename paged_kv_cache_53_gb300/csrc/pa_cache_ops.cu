@@ -151,7 +151,60 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant_
   for (int c = threadIdx.x; c < chunks_per_block; c += blockDim.x) d[c] = __ldg(s + c);
 }
 
+struct SwapPtrs {
+  const uint4* src_k[kMaxSwapLayers];
+  const uint4* src_v[kMaxSwapLayers];
+  uint4* dst_k[kMaxSwapLayers];
+  uint4* dst_v[kMaxSwapLayers];
+};
+
+// Whole-block copies from one pool to another (device memory or pinned host memory
+// reached through the unified address space): one CTA per (pair, layer, K-or-V).
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const __grid_constant__ SwapPtrs ptrs,
+                                                          const int32_t* __restrict__ pairs,
+                                                          int chunks_per_block, int src_blocks,
+                                                          int dst_blocks, int32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (threadIdx.x == 0 && blockIdx.z == 0) flag_status(status, PA_STATUS_BAD_BLOCK);
+    return;
+  }
+  const uint4* s = (blockIdx.z == 0 ? ptrs.src_k[layer] : ptrs.src_v[layer]) +
+                   (size_t)src * chunks_per_block;
+  uint4* d = (blockIdx.z == 0 ? ptrs.dst_k[layer] : ptrs.dst_v[layer]) +
+             (size_t)dst * chunks_per_block;
+  // four independent 16-byte loads in flight per thread: host memory is far away
+  int c = threadIdx.x;
+  for (; c + 3 * blockDim.x < chunks_per_block; c += 4 * blockDim.x) {
+    const uint4 a = s[c], b = s[c + blockDim.x], e = s[c + 2 * blockDim.x],
+                f = s[c + 3 * blockDim.x];
+    d[c] = a;
+    d[c + blockDim.x] = b;
+    d[c + 2 * blockDim.x] = e;
+    d[c + 3 * blockDim.x] = f;
+  }
+  for (; c < chunks_per_block; c += blockDim.x) d[c] = s[c];
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
+                               void* const* dst_v, int num_layers, const int32_t* pairs,
+                               int num_pairs, size_t block_bytes, int src_blocks,
+                               int dst_blocks, int32_t* status, cudaStream_t stream) {
+  SwapPtrs ptrs;
+  for (int l = 0; l < num_layers; ++l) {
+    ptrs.src_k[l] = static_cast<const uint4*>(src_k[l]);
+    ptrs.src_v[l] = static_cast<const uint4*>(src_v[l]);
+    ptrs.dst_k[l] = static_cast<uint4*>(dst_k[l]);
+    ptrs.dst_v[l] = static_cast<uint4*>(dst_v[l]);
+  }
+  return launch_pdl(swap_blocks_kernel, dim3(num_pairs, num_layers, 2), dim3(256), 0, stream,
+                    ptrs, pairs, (int)(block_bytes / 16), src_blocks, dst_blocks, status);
+}
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
                                 const int32_t* cu_q_lens, const int32_t* context_lens,

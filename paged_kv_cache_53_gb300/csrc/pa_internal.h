@@ -59,6 +59,12 @@ cudaError_t launch_cache_append(const void* k_new, const void* v_new, void* k_ca
                                 cudaStream_t stream);
 
 constexpr int kMaxCopyLayers = 256;
+constexpr int kMaxSwapLayers = 128;
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
+                               void* const* dst_v, int num_layers, const int32_t* pairs,
+                               int num_pairs, size_t block_bytes, int src_blocks,
+                               int dst_blocks, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                                const int32_t* pairs, int num_pairs, size_t block_bytes,
                                int num_blocks, int32_t* status, cudaStream_t stream);
