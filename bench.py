@@ -442,6 +442,73 @@ def run_ours(args, rank, world, local_rank):
     return res, step
 
 
+# ------------------------------------------------------------------ swap (pre-emption)
+def run_swap(args, local_rank):
+    """pa_swap_blocks bandwidth: a scattered set of blocks of a Llama-3.1-8B-shaped layer
+    (8 KV heads, head dim 128, block 16, bf16: 64 KiB of K+V per block) moved device ->
+    page-locked host and back, against one contiguous copy of the same bytes each way
+    (the host link's practical peak)."""
+    import torch
+    import paged_kv_cache_53_gb300 as pa
+    import paged_kv_cache_53_gb300.build as pabuild
+
+    pabuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nb_dev, nb_host, h_kv, bs, d = 16384, args.swap_blocks, 8, 16, 128
+    g = torch.Generator(device=dev).manual_seed(53_010)
+    kc = W.randn((nb_dev, h_kv, bs, d), "bf16", dev, g)
+    vc = W.randn((nb_dev, h_kv, bs, d), "bf16", dev, g)
+    hk = torch.empty((nb_host, h_kv, bs, d), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(53_010)
+    dev_ids = rng.permutation(nb_dev)[:nb_host].astype(np.int32)
+    out_pairs = torch.from_numpy(np.stack([dev_ids, np.arange(nb_host, dtype=np.int32)], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(nb_host, dtype=np.int32),
+                                          rng.permutation(nb_dev)[:nb_host].astype(np.int32)],
+                                         1)).to(dev)
+    nbytes = 2 * nb_host * h_kv * bs * d * 2  # K and V
+    stream = torch.cuda.current_stream(dev)
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = mk(), mk()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    with ClockSampler(local_rank) as clocks:
+        t_out = timed(lambda: pa.swap_blocks([kc], [vc], [hk], [hv], out_pairs))
+        t_in = timed(lambda: pa.swap_blocks([hk], [hv], [kc], [vc], in_pairs))
+        flat_d = kc[:nb_host]
+        flat_h = hk
+        t_d2h = timed(lambda: (flat_h.copy_(flat_d, non_blocking=True),
+                               hv.copy_(vc[:nb_host], non_blocking=True)))
+        t_h2d = timed(lambda: (flat_d.copy_(flat_h, non_blocking=True),
+                               vc[:nb_host].copy_(hv, non_blocking=True)))
+    if pa.get_status() != 0:
+        raise RuntimeError("library status word set during the swap measurement")
+    gbs = lambda ms: round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return {
+        "metric": "swap GB/s (device <-> page-locked host, scattered blocks)",
+        "value": gbs(t_out), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"swap {nb_host} blocks of 8x16x128 bf16 K+V, one layer",
+                   "bytes_per_direction": nbytes},
+        "swap_out_ms": round(t_out, 4), "swap_in_ms": round(t_in, 4),
+        "swap_out_gbs": gbs(t_out), "swap_in_gbs": gbs(t_in),
+        "contiguous_copy_d2h_gbs": gbs(t_d2h), "contiguous_copy_h2d_gbs": gbs(t_h2d),
+        "frac_of_contiguous_copy": {"out": round(t_d2h / t_out, 4), "in": round(t_h2d / t_in, 4)},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+    }
+
+
 # ------------------------------------------------------------------ oracle (CPU) timing
 def _oracle_worker(payload):
     """Runs the oracle decode over one chunk of sequences; returns (seconds, kv tokens)."""
@@ -607,6 +674,9 @@ def main():
     ap.add_argument("--ref-total-s", type=float, default=120.0,
                     help="wall seconds the reference arm's timed steps may take in total")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["step", "swap"], default="step",
+                    help="step: the hot path over --workload; swap: pa_swap_blocks bandwidth")
+    ap.add_argument("--swap-blocks", type=int, default=8192)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
@@ -614,6 +684,15 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.op == "swap":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the swap measurement has no oracle arm (a plain copy)"}))
+            return 0
+        if rank == 0:
+            print(json.dumps(run_swap(args, local_rank)), flush=True)
+        return 0
 
     if args.impl == "reference":
         if rank != 0:
