@@ -60,6 +60,8 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 #define PA_STATUS_BAD_SLOT 0x2    /* a slot outside [0, num_blocks * block_size) */
 #define PA_STATUS_BAD_CONTEXT 0x4 /* context < 0, or longer than max_ctx / its table */
 #define PA_STATUS_TIMEOUT 0x8     /* a pipeline wait in a kernel gave up (never expected) */
+#define PA_STATUS_RANGE 0x10      /* chunked prefill met a bf16 V value of magnitude >= 65520,
+                                     outside fp16's range (see pa_prefill_chunk) */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pa_version(void);
@@ -297,7 +299,10 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int n
  *   cu_q_lens     int32 [num_seqs + 1]; max_q >= every chunk length
  *   context_lens  int32 [num_seqs]; chunk_len <= context_lens[b] <= max_ctx
  *   workspace     device scratch of pa_prefill_workspace_bytes(...) bytes (may be 0)
- * QK^T and PV run on the tensor cores with fp32 accumulation.
+ * QK^T and PV run on the tensor cores with fp32 accumulation.  P and V enter the PV
+ * product in fp16 (unit roundoff 2^-11; bf16's 2^-8 alone would not meet a 2e-3 bound):
+ * bf16 V values are converted to fp16 in shared memory, which is exact below 65520 in
+ * magnitude; a larger V value sets PA_STATUS_RANGE (its products are not exact).
  */
 int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
                      const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,

@@ -238,6 +238,19 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // Named barrier over a subset of the CTA's warps.
+// Named barrier over `threads` threads that also returns whether `pred` held for all of
+// them (so that a group can leave a loop together).
+__device__ __forceinline__ bool named_barrier_and(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -16,15 +16,19 @@
 //   warp 1     MMA issuer (one thread): S_x(j) = Q_x K_j^T into TMEM, then
 //              O_x += P_x(j) V_j with P read from TMEM, in the order PV_A(j), S_A(j+1),
 //              PV_B(j), S_B(j+1), so that one tile's softmax overlaps the other tile's
-//              products.  P is carried as the sum of a bf16/fp16 "hi" term and its
-//              rounding residual "lo" (two MMAs): a single 16-bit P alone can miss a 2e-3
-//              absolute tolerance on short contexts.
+//              products.  PV runs in fp16: P rounded to fp16 has a unit roundoff of
+//              2^-11, which keeps the output within a 2e-3 absolute bound where bf16's
+//              2^-8 would not.  S = Q K^T runs in the input type.
 //   warps 4-11 two softmax warpgroups, one per query tile, one thread per row: read
-//              S from TMEM, apply scale and the causal mask, keep the running max
-//              (moved only when it grows by more than 2^8, rescaling O in TMEM then) and
-//              sum, write P over S's own TMEM columns; at the end normalise O and store.
-// Tiles wholly above the diagonal are never loaded; only the last K/V tile can hold
-// positions past the context, whose V rows are zeroed before they meet P = 0.
+//              the row of S from TMEM into registers, apply scale and the causal mask,
+//              keep the running max (moved only when it grows by more than 2^8,
+//              rescaling O in TMEM then) and sum, write P as fp16 over S's own TMEM
+//              columns; at the end normalise O and store.  While the tensor core works,
+//              each warpgroup also converts half of the next K/V tile's V from bf16 to
+//              fp16 in place (exact below 65520 in magnitude; larger values are flagged)
+//              and zeroes the V rows past the context, which would otherwise meet P = 0
+//              with whatever bits they hold.  One conversion serves both query tiles.
+// Tiles wholly above the diagonal are never loaded.
 #include <algorithm>
 #include <mutex>
 
@@ -67,10 +71,14 @@ struct PrefillCfg {
   static constexpr int kStageBytes = 2 * kKBytes;      // K then V
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kBlocksPerTile = BN / BS;
-  static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 x softmax WG
+  static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 softmax WGs
+  static constexpr int kVThreads = 256;                // both softmax WGs convert V
   static constexpr int kTmemCols = 512;                // S/P_A | S/P_B | O_A | O_B
-  // barriers: q_full, kv_full[S], kv_empty[S], then per query tile s_full, p_full, pv_done
-  static constexpr int kBars = 1 + 2 * kStages + 3 * kTiles;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_ready[S], then per
+  // query tile s_full, p_full, pv_done.  K and V of a stage have barriers of their own:
+  // K(j) is done with once S(j) has been computed, an iteration before P(j) V(j), so the
+  // next K tile can load that much earlier.
+  static constexpr int kBars = 1 + 5 * kStages + 3 * kTiles;
   static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
                                   kBars * 8 + 16;
 };
@@ -204,9 +212,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 1 + S;
-  uint64_t* s_full = bars + 1 + 2 * S;  // [tile]
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 1 + S;
+  uint64_t* v_full = bars + 1 + 2 * S;
+  uint64_t* v_empty = bars + 1 + 3 * S;
+  uint64_t* v_ready = bars + 1 + 4 * S;  // V of the stage converted to fp16
+  uint64_t* s_full = bars + 1 + 5 * S;   // [tile]
   uint64_t* p_full = s_full + NT;
   uint64_t* pv_done = p_full + NT;
 
@@ -241,8 +252,11 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(q_full), 1);
     for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(kv_full + i), 1);
-      mbar_init(smem_addr(kv_empty + i), 1);
+      mbar_init(smem_addr(k_full + i), 1);
+      mbar_init(smem_addr(k_empty + i), 1);
+      mbar_init(smem_addr(v_full + i), 1);
+      mbar_init(smem_addr(v_empty + i), 1);
+      mbar_init(smem_addr(v_ready + i), C::kVThreads);
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(smem_addr(s_full + x), 1);
@@ -264,9 +278,8 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S of tile x at x * BN (P_x is written over it), O of tile x at
-  // NT * BN + x * D.  P layout: 32-token chunk c of the row holds its 16-bit hi terms in
-  // columns 32c .. 32c+15 and its lo terms in 32c+16 .. 32c+31 (two tokens per column).
+  // TMEM columns: S of tile x at x * BN (P_x is written over its first half: token t of
+  // the K/V tile in column t / 2, two fp16 per column), O of tile x at NT * BN + x * D.
   bool ok = true;
 
   if (warp == 0) {
@@ -289,7 +302,6 @@ __global__ void __launch_bounds__(384, 1)
     const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
     for (int j = 0; j < n_kv && ok; ++j) {
       const int s = j % S;
-      if (!mbar_wait(smem_addr(kv_empty + s), ((j / S) & 1) ^ 1)) { ok = false; break; }
       const int bi = j * C::kBlocksPerTile + lane;
       int id = -1;
       if (lane < C::kBlocksPerTile && bi < nblk_ctx) {
@@ -299,20 +311,25 @@ __global__ void __launch_bounds__(384, 1)
           id = -1;
         }
       }
-      uint8_t* st = sKV + s * C::kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(smem_addr(kv_full + s), C::kStageBytes);
+      // K of tile j, then its V, each once its slot's previous tile is done with
 #pragma unroll
-      for (int i = 0; i < C::kBlocksPerTile; ++i) {
-        const int idi = __shfl_sync(~0u, id, i);
-        if (lane == 0) {
-          // blocks past the context (and bad ids) read a box wholly outside: zeros
-          const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
+      for (int kv = 0; kv < 2; ++kv) {
+        uint64_t* full = kv == 0 ? k_full : v_full;
+        uint64_t* empty = kv == 0 ? k_empty : v_empty;
+        if (!mbar_wait(smem_addr(empty + s), ((j / S) & 1) ^ 1)) { ok = false; break; }
+        uint8_t* st = sKV + s * C::kStageBytes + kv * C::kKBytes;
+        const CUtensorMap* map = kv == 0 ? &tmk : &tmv;
+        if (lane == 0) mbar_arrive_expect_tx(smem_addr(full + s), C::kKBytes);
 #pragma unroll
-          for (int hb = 0; hb < C::kHalves; ++hb) {
-            const int off = hb * C::kKvHalfBytes + i * BS * 128;
-            tma_load_2d(smem_addr(st + off), &tmk, hb * 64, y, smem_addr(kv_full + s), keep);
-            tma_load_2d(smem_addr(st + C::kKBytes + off), &tmv, hb * 64, y,
-                        smem_addr(kv_full + s), keep);
+        for (int i = 0; i < C::kBlocksPerTile; ++i) {
+          const int idi = __shfl_sync(~0u, id, i);
+          if (lane == 0) {
+            // blocks past the context (and bad ids) read a box wholly outside: zeros
+            const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
+#pragma unroll
+            for (int hb = 0; hb < C::kHalves; ++hb)
+              tma_load_2d(smem_addr(st + hb * C::kKvHalfBytes + i * BS * 128), map, hb * 64, y,
+                          smem_addr(full + s), keep);
           }
         }
       }
@@ -326,7 +343,7 @@ __global__ void __launch_bounds__(384, 1)
     // execute in order, so no wait is needed between the two.
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM, BN, false, false);
-      const uint32_t id_o = tc::idesc_f16(Fmt<T>::v, C::BM, D, false, true);
+      const uint32_t id_o = tc::idesc_f16(Fmt<__half>::v, C::BM, D, false, true);  // fp16 P, V
       auto issue_s = [&](int x, int j) {
         const uint32_t tS = tmem + x * BN;
         const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
@@ -340,28 +357,32 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc::commit(smem_addr(s_full + x));
       };
+      int v_seen = -1;  // last K/V tile whose fp16 V was waited for
       auto issue_pv = [&](int x, int j) -> bool {
         if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
+        if (v_seen < j) {
+          if (!mbar_wait(smem_addr(v_ready + j % S), (j / S) & 1)) return false;
+          v_seen = j;
+        }
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
         const uint32_t sv = smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
           const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
-          tc::mma_f16_ts(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
-          tc::mma_f16_ts(tO, tP + col + 16, bdesc, id_o, true);
+          tc::mma_f16_ts(tO, tP + 8 * ks, bdesc, id_o, j > 0 || ks > 0);
         }
         tc::commit(smem_addr(pv_done + x));
         return true;
       };
-      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(kv_full), 0)) ok = false;
+      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(k_full), 0)) ok = false;
       if (ok) {
         tc::fence_after_sync();
 #pragma unroll
         for (int x = 0; x < NT; ++x)
           if (tg[x].n_kv > 0) issue_s(x, 0);
+        tc::commit(smem_addr(k_empty));  // K(0) is read once both S(0) are done
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         bool next_ready = false;
@@ -370,14 +391,15 @@ __global__ void __launch_bounds__(384, 1)
           if (j < tg[x].n_kv && !issue_pv(x, j)) { ok = false; break; }
           if (j + 1 < tg[x].n_kv) {
             if (!next_ready) {
-              if (!mbar_wait(smem_addr(kv_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
+              if (!mbar_wait(smem_addr(k_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
               tc::fence_after_sync();
               next_ready = true;
             }
             issue_s(x, j + 1);
           }
         }
-        tc::commit(smem_addr(kv_empty + j % S));
+        tc::commit(smem_addr(v_empty + j % S));                   // V(j): both PV(j) issued
+        if (j + 1 < n_kv) tc::commit(smem_addr(k_empty + (j + 1) % S));  // K(j+1): both S
       }
       if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
@@ -393,59 +415,103 @@ __global__ void __launch_bounds__(384, 1)
     const int rpos = ctx0 + g.t0 + r / G;                    // position of this row's query
     const int rpos_warp = ctx0 + g.t0 + (r & ~31) / G;       // smallest position in the warp
     const float sc = p.scale_log2;
+    // V of K/V tile jv: bf16 -> fp16 in place and rows past the context zeroed, this
+    // thread taking every 256th 16-byte piece
+    const int vt = threadIdx.x - 128;
+    __half2 vmax = __floats2half2_rn(0.f, 0.f);  // largest |v| converted, per lane half
+    auto convert_v = [&](int jv) -> bool {
+      const int s = jv % S;
+      if (!mbar_wait(smem_addr(v_full + s), (jv / S) & 1)) return false;
+      const int z0 = ctx - jv * BN;  // rows from z0 on lie past the context
+      uint4* sv = reinterpret_cast<uint4*>(sKV + s * C::kStageBytes + C::kKBytes);
+      constexpr int kPer = C::kKBytes / 16 / C::kVThreads;
+      uint4 v[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) v[u] = sv[vt + u * C::kVThreads];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        // a piece's row: rows are 128 bytes in every 64-column half (the swizzle only
+        // permutes pieces within a row); pieces past the context become zeros
+        const int i = vt + u * C::kVThreads;
+        if (z0 < BN && ((i % (C::kKvHalfBytes / 16)) >> 3) >= z0) {
+          v[u] = make_uint4(0, 0, 0, 0);
+        } else if constexpr (Fmt<T>::v == 1) {
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16),
+                                                 __uint_as_float(w[k] & 0xffff0000u));
+            vmax = __hmax2(vmax, __habs2(hv));
+            w[k] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) sv[vt + u * C::kVThreads] = v[u];
+      tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+      mbar_arrive(smem_addr(v_ready + s));
+      return true;
+    };
     float m = kNegInf, l = 0.f;
-    for (int j = 0; j < g.n_kv; ++j) {
+    if (n_kv > 0 && !convert_v(0)) ok = false;
+    for (int j = 0; j < g.n_kv && ok; ++j) {
       if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       const int kp0 = j * BN;
       const bool full = kp0 + BN - 1 <= rpos_warp;  // below the diagonal for the whole warp
-      // pass 1: row maximum of scale * S over the visible positions
-      float mx = kNegInf;
+      // the row's scores, loaded behind one wait
+      static_assert(BN == 128, "a 128-column row in registers");
+      float c[4][32];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        float a[32], bq[32];
-        tc::tmem_ld32(tS + c0, a);
-        tc::tmem_ld32(tS + c0 + 32, bq);
-        tc::tmem_wait_ld();
-        if (full) {
+      for (int k = 0; k < 4; ++k) tc::tmem_ld32(tS + 32 * k, c[k]);
+      tc::tmem_wait_ld();
+      // row maximum of scale * S over the visible positions
+      float mx;
+      if (full && sc > 0.f) {
+        float rm[4];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(a[i], bq[i]) * sc);
-        } else {
+        for (int k = 0; k < 4; ++k) {
+          rm[k] = c[k][0];
+#pragma unroll
+          for (int i = 1; i < 32; ++i) rm[k] = fmaxf(rm[k], c[k][i]);
+        }
+        mx = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3])) * sc;
+      } else if (full) {
+        mx = kNegInf;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, c[k][i] * sc);
+      } else {
+        // on the diagonal the scores are scaled in place and masked positions set to -inf
+        mx = kNegInf;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            mx = fmaxf(mx, kp0 + c0 + i <= rpos ? a[i] * sc : kNegInf);
-            mx = fmaxf(mx, kp0 + c0 + 32 + i <= rpos ? bq[i] * sc : kNegInf);
+            c[k][i] = kp0 + 32 * k + i <= rpos ? c[k][i] * sc : kNegInf;
+            mx = fmaxf(mx, c[k][i]);
           }
-        }
       }
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
-      // pass 2: P = 2^(scale * S - m) as hi + lo 16-bit terms, over S's own columns
-      float sum = 0.f;
+      // P = 2^(scale * S - m) in fp16, tokens 32k .. 32k+31 into columns 16k .. 16k+15
+      // (the scores there are already in registers)
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float a[32];
-        tc::tmem_ld32(tS + c0, a);
-        tc::tmem_wait_ld();
-        if (full) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            a[i] = kp0 + c0 + i <= rpos ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
-        }
-        uint32_t hi[16], lo[16];
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          sum += a[2 * i] + a[2 * i + 1];
-          hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+          const float e0 = fast_exp2(full ? fmaf(c[k][2 * i], sc, -m) : c[k][2 * i] - m);
+          const float e1 = fast_exp2(full ? fmaf(c[k][2 * i + 1], sc, -m) : c[k][2 * i + 1] - m);
+          s2[i & 3] += e0 + e1;
+          pk[i] = Mma<__half>::pack(e0, e1);
         }
-        tc::tmem_st16(tS + c0, hi);
-        tc::tmem_st16(tS + c0 + 16, lo);
+        tc::tmem_st16(tS + 16 * k, pk);
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((s2[0] + s2[1]) + (s2[2] + s2[3]));
       if (j >= 1 && __any_sync(~0u, need)) {
         // O holds P_0..j-1 V: once the last of those products is done, rescale it
         if (!mbar_wait(smem_addr(pv_done + x), (j - 1) & 1)) { ok = false; break; }
@@ -460,24 +526,19 @@ __global__ void __launch_bounds__(384, 1)
           tc::tmem_st32(tO + c0, o);
         }
       }
-      // V rows of the context's last K/V tile past the context (inside its last block)
-      // may hold anything, NaN bits included, and would meet P = 0: zero them.  Both
-      // warpgroups may do it; they write the same zeros.
-      const int z0 = ctx - kp0, z1 = min(BN, nblk_ctx * BS - kp0);
-      if (z0 < z1) {
-        const int s = j % S;
-        if (!mbar_wait(smem_addr(kv_full + s), (j / S) & 1)) { ok = false; break; }
-        const uint32_t sv = smem_addr(sKV + s * C::kStageBytes + C::kKBytes);
-        for (int i = r; i < (z1 - z0) * (D / 8); i += 128) {
-          const int vr = z0 + i / (D / 8), c = i % (D / 8);
-          st_shared_v4(sv + (c >> 3) * C::kKvHalfBytes + vr * 128 + (c & 7) * 16,
-                       make_uint4(0, 0, 0, 0));
-        }
-        tc::fence_proxy_async_smem();
-      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(smem_addr(p_full + x));
+      if (j + 1 < n_kv && !convert_v(j + 1)) { ok = false; break; }
+    }
+    // the CTA's K/V tiles past this tile's last (the other tile reaches further) still
+    // need this warpgroup's half of their conversion
+    for (int jv = g.n_kv + 1; jv < n_kv && ok; ++jv)
+      if (!convert_v(jv)) ok = false;
+    if constexpr (Fmt<T>::v == 1) {
+      // a value at or above 65520 in magnitude became inf (NaN stays NaN): flag it
+      const float2 vm = __half22float2(vmax);
+      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) flag_status(p.status, PA_STATUS_RANGE);
     }
     // epilogue: O / l -> out rows
     if (ok && g.n_kv > 0 && mbar_wait(smem_addr(pv_done + x), (g.n_kv - 1) & 1)) {

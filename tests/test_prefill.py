@@ -92,6 +92,21 @@ def test_prefill_nan_past_context_is_ignored(pa):
     assert max_abs_err(got, ref["out_prefill"]) <= TOL["bf16"]
 
 
+def test_prefill_v_beyond_fp16_range_is_flagged(pa):
+    """P V runs in fp16: a bf16 V value of magnitude >= 65520 cannot be converted exactly
+    and sets the range status bit; values just inside fp16's range stay exact."""
+    step = W.prefill_step("prange", W.Shape(8, 2, 128, 16, "bf16"), [40], [8], seed=36)
+    run = StepRun(step)
+    blk = int(step.prefill.block_tables[0, 0])
+    run.vals["v_cache"][blk, 0, 3, 5] = 65280.0  # the largest bf16 below 65520
+    run.run()
+    assert pa.get_status() == 0
+    run = StepRun(step)
+    run.vals["v_cache"][blk, 1, 2, 7] = -1.0e5
+    run.run()
+    assert pa.get_status() & pa.STATUS_RANGE
+
+
 def test_mixed_prefill_full_size_sampled(pa):
     """The mixed workload's prefill batch at full size (8 chunks of 512 over up to 16,384
     context tokens, block size 32), compared on sampled rows of every sequence that
