@@ -509,6 +509,75 @@ def run_swap(args, local_rank):
     }
 
 
+# ------------------------------------------------------------------ block manager (host)
+def _blockmgr_trace(bm, n_steps: int, rng_seed: int = 53_020):
+    """One serving-like trace through a block manager: 128 requests on a shared
+    2,048-token system prompt (prefix caching) plus 8 prompts with 4 samples each, then
+    `n_steps` decode steps in which every sequence appends one token and the step's
+    copy-on-write pairs, tables and slots are emitted; every 64 steps 16 requests finish
+    and 16 new ones arrive.  Returns seconds spent in the decode steps."""
+    import time
+    rng = np.random.default_rng(rng_seed)
+    system = rng.integers(0, 50_000, 2048).tolist()
+    live, nxt = [], 0
+    for _ in range(128):
+        bm.add_sequence(nxt, system + rng.integers(0, 50_000, int(rng.integers(1, 513))).tolist())
+        live.append(nxt)
+        nxt += 1
+    for _ in range(8):
+        parent = nxt
+        bm.add_sequence(parent, rng.integers(0, 50_000, int(rng.integers(1, 513))).tolist())
+        live.append(parent)
+        nxt += 1
+        for _ in range(3):
+            bm.fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+    width = 256
+    tok = rng.integers(0, 50_000, size=len(live)).tolist()
+    t = 0.0
+    for step in range(n_steps):
+        t0 = time.perf_counter()
+        bm.append_tokens_batch(live, tok[:len(live)])
+        bm.take_copies()
+        bm.block_tables(live, width)
+        bm.slot_mapping(live, [1] * len(live))
+        t += time.perf_counter() - t0
+        if step % 64 == 63:
+            for s in live[:16]:
+                bm.free_sequence(s)
+            live = live[16:]
+            for _ in range(16):
+                bm.add_sequence(nxt, system + rng.integers(0, 50_000, int(rng.integers(1, 513))).tolist())
+                live.append(nxt)
+                nxt += 1
+    return t
+
+
+def run_blockmgr(args):
+    """Host bookkeeping per decode step of 160 sequences: the C++ block manager against
+    the reference block manager on the same trace."""
+    import paged_kv_cache_53_gb300.build as pabuild
+    pabuild.build()
+    from paged_kv_cache_53_gb300.block_manager import BlockManager
+    from oracle.block_manager import BlockManager as RefManager  # the reference arm
+    nb, steps = 40_000, args.steps
+    t_ours = _blockmgr_trace(BlockManager(nb, 16, prefix_caching=True), steps)
+    ref_steps = max(1, min(steps, 64))
+    t_ref = _blockmgr_trace(RefManager(nb, 16, prefix_caching=True), ref_steps)
+    us = lambda t, n: round(t / n * 1e6, 2)
+    return {
+        "metric": "block manager host time per decode step (160 sequences)",
+        "value": us(t_ours, steps), "unit": "us/step", "higher_is_better": False,
+        "n_gpus": 0, "steps": steps, "warmup": 0, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": "128 requests on a 2,048-token shared prompt + 8 x 4 samples, "
+                               "one token each per step, block 16, prefix caching on",
+                   "per_step": "append 160 tokens, take copy pairs, emit tables and slots"},
+        "cpu_baseline": {"value": us(t_ref, ref_steps), "unit": "us/step", "cores": 1,
+                         "kind": "oracle", "sample": f"{ref_steps} steps of the same trace"},
+    }
+
+
 # ------------------------------------------------------------------ oracle (CPU) timing
 def _oracle_worker(payload):
     """Runs the oracle decode over one chunk of sequences; returns (seconds, kv tokens)."""
@@ -674,8 +743,9 @@ def main():
     ap.add_argument("--ref-total-s", type=float, default=120.0,
                     help="wall seconds the reference arm's timed steps may take in total")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["step", "swap"], default="step",
-                    help="step: the hot path over --workload; swap: pa_swap_blocks bandwidth")
+    ap.add_argument("--op", choices=["step", "swap", "blockmgr"], default="step",
+                    help="step: the hot path over --workload; swap: pa_swap_blocks bandwidth; "
+                         "blockmgr: host block-manager time per decode step")
     ap.add_argument("--swap-blocks", type=int, default=8192)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -684,6 +754,15 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.op == "blockmgr":
+        if rank == 0 and args.impl == "ours":
+            print(json.dumps(run_blockmgr(args)), flush=True)
+        elif rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the block-manager measurement reports the reference manager "
+                              "in its cpu_baseline"}))
+        return 0
 
     if args.op == "swap":
         if args.impl == "reference":

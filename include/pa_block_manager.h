@@ -91,6 +91,13 @@ int pa_bm_add_sequence(pa_block_manager* bm, int64_t seq_id, const int32_t* toke
  * a shared last block first (the pair is queued for pa_bm_take_copies). */
 int pa_bm_append_tokens(pa_block_manager* bm, int64_t seq_id, const int32_t* tokens, int n);
 
+/* pa_bm_append_tokens for n distinct sequences in one call, in the order given: sequence
+ * seq_ids[i] appends counts[i] tokens (counts may be null: one each) taken in turn from
+ * tokens.  All or nothing: PA_ERR_NO_BLOCKS (or PA_ERR_INVALID_ARG for an unknown,
+ * swapped-out or repeated sequence) leaves every sequence as it was. */
+int pa_bm_append_tokens_batch(pa_block_manager* bm, const int64_t* seq_ids, int n,
+                              const int32_t* tokens, const int32_t* counts);
+
 /* child_id reads every block of parent_id (parallel sampling, beam search). */
 int pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id);
 

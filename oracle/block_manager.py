@@ -201,6 +201,36 @@ class BlockManager:
             if (pos + 1) % self.bs == 0:
                 self._on_full(seq, pos // self.bs)
 
+    def append_tokens_batch(self, seq_ids: Sequence[int], tokens: Sequence[int],
+                            counts: Optional[Sequence[int]] = None):
+        """append_tokens for each listed sequence in turn (one token each unless
+        `counts` says otherwise), all or nothing: the blocks the whole batch takes are
+        counted first, copies included (a copy leaves its source with one reader fewer,
+        so a later sequence of the batch on the same block may append in place)."""
+        counts = [1] * len(seq_ids) if counts is None else list(counts)
+        if len(set(seq_ids)) != len(seq_ids):
+            raise ValueError("a sequence is listed twice")
+        need, copied = 0, {}
+        for s, k in zip(seq_ids, counts):
+            seq = self.seqs[s]
+            if seq.swapped:
+                raise RuntimeError(f"sequence {s} is swapped out")
+            if k == 0:
+                continue
+            n0 = len(seq.tokens)
+            need += -(-(n0 + k) // self.bs) - -(-n0 // self.bs)
+            if n0 % self.bs != 0:
+                last = seq.blocks[-1]
+                if self.ref[last] - copied.get(last, 0) > 1:
+                    need += 1
+                    copied[last] = copied.get(last, 0) + 1
+        if need > len(self.queue):
+            raise NoBlocks("not enough free blocks to append")
+        pos = 0
+        for s, k in zip(seq_ids, counts):
+            self.append_tokens(s, tokens[pos:pos + k])
+            pos += k
+
     def fork(self, parent_id: int, child_id: int):
         """The child reads every block of the parent (parallel sampling, beam search)."""
         if child_id in self.seqs:

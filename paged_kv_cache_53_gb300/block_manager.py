@@ -27,6 +27,7 @@ _SIGNATURES = {
     "pa_bm_can_allocate": ([_p, _i, _i], _i),
     "pa_bm_add_sequence": ([_p, _i64, _p, _i, _p, _i, _p], _i),
     "pa_bm_append_tokens": ([_p, _i64, _p, _i], _i),
+    "pa_bm_append_tokens_batch": ([_p, _p, _i, _p, _p], _i),
     "pa_bm_fork": ([_p, _i64, _i64], _i),
     "pa_bm_free_sequence": ([_p, _i64], _i),
     "pa_bm_take_copies": ([_p, _p, _i, _p], _i),
@@ -121,6 +122,23 @@ class BlockManager:
     def append_tokens(self, seq_id: int, tokens: Sequence[int]):
         t, tp = _arr(tokens, np.int32)
         _check(_lib().pa_bm_append_tokens(self._h, seq_id, tp, t.size))
+
+    def append_tokens_batch(self, seq_ids: Sequence[int], tokens: Sequence[int],
+                            counts: Sequence[int] = None):
+        """Sequence seq_ids[i] appends counts[i] tokens (default one each), taken in turn
+        from `tokens`; all or nothing."""
+        s, sp = _arr(seq_ids, np.int64)
+        t, tp = _arr(tokens, np.int32)
+        if counts is None:
+            cp = None
+            total = s.size
+        else:
+            c, cp = _arr(counts, np.int32)
+            self._keep_c = c
+            total = int(c.sum())
+        if t.size != total:
+            raise ValueError(f"{t.size} tokens for {total} appends")
+        _check(_lib().pa_bm_append_tokens_batch(self._h, sp, s.size, tp, cp))
 
     def fork(self, parent_id: int, child_id: int):
         _check(_lib().pa_bm_fork(self._h, parent_id, child_id))

@@ -42,6 +42,7 @@ struct Seq {
   int64_t tokens = 0;
   std::string extra;
   bool swapped = false;
+  uint64_t batch = 0;  // last batched call that listed the sequence
 };
 
 }  // namespace
@@ -60,6 +61,9 @@ struct pa_block_manager {
   std::vector<int32_t> host_ref;
   std::unordered_map<int64_t, Seq> seqs;
   std::vector<int32_t> copies;  // (src, dst) flattened
+  uint64_t batches = 0;         // batched calls so far
+  std::vector<Seq*> batch_seqs;
+  std::vector<std::pair<int32_t, int32_t>> batch_copied;  // source block, copies counted
 
   pa_block_manager(int num_blocks, int block_size, bool prefix_caching, int num_host)
       : nb(num_blocks), bs(block_size), caching(prefix_caching), next(num_blocks + 1),
@@ -123,6 +127,33 @@ struct pa_block_manager {
       cached.emplace(k, b);
       key[b] = k;
       has_key[b] = 1;
+    }
+  }
+
+  // Appends n tokens to s; the caller has checked that the pool can supply the blocks.
+  void append(Seq& s, const int32_t* toks, int n) {
+    for (int i = 0; i < n; ++i) {
+      const int64_t pos = s.tokens;
+      if (pos % bs == 0) {
+        s.blocks.push_back(take());
+      } else if (ref[s.blocks.back()] > 1) {  // copy-on-write
+        const int32_t src = s.blocks.back();
+        const int32_t dst = take();
+        copies.push_back(src);
+        copies.push_back(dst);
+        --ref[src];
+        s.blocks.back() = dst;
+      }
+      s.tail.push_back(toks[i]);
+      ++s.tokens;
+      if ((pos + 1) % bs == 0) {
+        if (caching) {
+          const size_t bi = (size_t)(pos / bs);
+          const Key k = block_key(bi ? &s.keys[bi - 1] : nullptr, s.tail.data(), s.extra);
+          on_full(s, bi, k);
+        }
+        s.tail.clear();
+      }
     }
   }
 
@@ -236,28 +267,60 @@ int pa_bm_append_tokens(pa_block_manager* bm, int64_t seq_id, const int32_t* tok
   if (need > bm->queued)
     return pa::fail(PA_ERR_NO_BLOCKS, "pa_bm_append_tokens: %lld blocks needed, %d free",
                     (long long)need, bm->queued);
+  bm->append(*s, tokens, n);
+  return PA_OK;
+}
+
+int pa_bm_append_tokens_batch(pa_block_manager* bm, const int64_t* seq_ids, int n,
+                              const int32_t* tokens, const int32_t* counts) {
+  pa::clear_error();
+  if (!bm || n < 0 || (n > 0 && !seq_ids))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_bm_append_tokens_batch: bad arguments");
+  // dry run: every sequence resident and listed once, and the blocks the whole batch
+  // takes, copies included (a copy lowers its source's reference count, so later
+  // sequences in the batch may append in place)
+  const uint64_t stamp = ++bm->batches;
+  bm->batch_seqs.resize(n);
+  bm->batch_copied.clear();
+  int64_t need = 0, total = 0;
   for (int i = 0; i < n; ++i) {
-    const int64_t pos = s->tokens;
-    if (pos % bs == 0) {
-      s->blocks.push_back(bm->take());
-    } else if (bm->ref[s->blocks.back()] > 1) {  // copy-on-write
-      const int32_t src = s->blocks.back();
-      const int32_t dst = bm->take();
-      bm->copies.push_back(src);
-      bm->copies.push_back(dst);
-      --bm->ref[src];
-      s->blocks.back() = dst;
-    }
-    s->tail.push_back(tokens[i]);
-    ++s->tokens;
-    if ((pos + 1) % bs == 0) {
-      if (bm->caching) {
-        const size_t bi = (size_t)(pos / bs);
-        const Key k = bm->block_key(bi ? &s->keys[bi - 1] : nullptr, s->tail.data(), s->extra);
-        bm->on_full(*s, bi, k);
+    Seq* s = bm->resident(seq_ids[i], "pa_bm_append_tokens_batch");
+    if (!s) return PA_ERR_INVALID_ARG;
+    if (s->batch == stamp)
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_bm_append_tokens_batch: sequence %lld repeated",
+                      (long long)seq_ids[i]);
+    s->batch = stamp;
+    const int k = counts ? counts[i] : 1;
+    if (k < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_bm_append_tokens_batch: negative count");
+    bm->batch_seqs[i] = s;
+    total += k;
+    if (k == 0) continue;
+    const int64_t n0 = s->tokens;
+    need += cdiv(n0 + k, bm->bs) - cdiv(n0, bm->bs);
+    if (n0 % bm->bs != 0 && bm->ref[s->blocks.back()] > 1) {  // shared partly filled block
+      const int32_t last = s->blocks.back();
+      int32_t c = 0;
+      for (auto& bc : bm->batch_copied)
+        if (bc.first == last) c = bc.second;
+      if (bm->ref[last] - c > 1) {
+        ++need;
+        bool found = false;
+        for (auto& bc : bm->batch_copied)
+          if (bc.first == last) { ++bc.second; found = true; }
+        if (!found) bm->batch_copied.emplace_back(last, 1);
       }
-      s->tail.clear();
     }
+  }
+  if (total > 0 && !tokens)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_bm_append_tokens_batch: null tokens");
+  if (need > bm->queued)
+    return pa::fail(PA_ERR_NO_BLOCKS, "pa_bm_append_tokens_batch: %lld blocks needed, %d free",
+                    (long long)need, bm->queued);
+  const int32_t* t = tokens;
+  for (int i = 0; i < n; ++i) {
+    const int k = counts ? counts[i] : 1;
+    bm->append(*bm->batch_seqs[i], t, k);
+    t += k;
   }
   return PA_OK;
 }

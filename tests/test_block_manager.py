@@ -90,6 +90,13 @@ def test_random_traces_match_the_reference(bmmod, caching, bs, nb, seed):
             toks = rng.integers(0, 3, int(rng.integers(1, 2 * bs + 2))).tolist()
             _both(lambda: bm.append_tokens(s, toks), lambda: ref.append_tokens(s, toks),
                   bmmod.NoBlocks)
+        elif op == 7 and len(resident) > 1 and rng.random() < 0.5:
+            grp = rng.choice(resident, size=min(len(resident), int(rng.integers(2, 6))),
+                             replace=False).tolist()
+            cnt = rng.integers(0, bs + 2, size=len(grp)).tolist()
+            toks = rng.integers(0, 3, int(sum(cnt))).tolist()
+            _both(lambda: bm.append_tokens_batch(grp, toks, cnt),
+                  lambda: ref.append_tokens_batch(grp, toks, cnt), bmmod.NoBlocks)
         elif op == 3 and resident:
             s = resident[int(rng.integers(len(resident)))]
             bm.fork(s, nxt)
@@ -145,6 +152,26 @@ def test_admission_of_the_measured_capacity(bmmod):
     assert n == 34
     with pytest.raises(bmmod.NoBlocks):
         bm.add_sequence(99, list(range(640)))
+
+
+def test_batch_append_copies_for_all_but_the_last_reader(bmmod):
+    """One decode step of four samples on a partly filled shared block, in one call:
+    three copies, the last sample appends in place; a shortage changes nothing."""
+    bm = bmmod.BlockManager(8, 16)
+    ref = RefManager(8, 16)
+    for m in (bm, ref):
+        m.add_sequence(0, list(range(37)))
+        for c in (1, 2, 3):
+            m.fork(0, c)
+        m.append_tokens_batch([1, 2, 3, 0], [7, 8, 9, 10])
+    assert bm.take_copies().tolist() == [list(p) for p in ref.take_copies()]
+    assert len(ref.copies) == 0 and bm.num_free_blocks() == ref.num_free_blocks() == 2
+    before = [bm.block_table(s) for s in range(4)]
+    with pytest.raises(bmmod.NoBlocks):  # 4 x 12 more tokens need 4 blocks, 2 are free
+        bm.append_tokens_batch([0, 1, 2, 3], [1] * 48, [12, 12, 12, 12])
+    assert [bm.block_table(s) for s in range(4)] == before
+    with pytest.raises(bmmod.PaError):
+        bm.append_tokens_batch([0, 0], [1, 2])
 
 
 def test_errors(bmmod):
