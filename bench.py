@@ -257,29 +257,37 @@ def run_ours(args, rank, world, local_rank):
     q_in = {kind: vals[f"q_{kind}"] for kind in meta}
     launches_per_step = 0
 
-    def one_step(ev=None):
-        """The whole hot path over one batch; ev = (decode start/end, prefill start/end)."""
+    # a step's inputs and outputs: per batch kind the query, new K/V and table tensors
+    resident_io = {kind: {"q": q_in[kind], "kn": vals[f"k_new_{kind}"],
+                          "vn": vals[f"v_new_{kind}"], **m} for kind, m in meta.items()}
+    resident_io["out"] = {"decode": out_dec if d is not None else None,
+                          "prefill": out_pre if p is not None else None}
+
+    def one_step(ev=None, io=None):
+        """The whole hot path over one batch; ev = (decode start/end, prefill start/end);
+        io = the step's input and output tensors (the resident ones by default)."""
         nonlocal launches_per_step
+        io = io or resident_io
         n = 0
         if pairs is not None:
             pa.copy_blocks([kc], [vc], pairs)
             n += 1
-        for kind, m in meta.items():  # slot mapping + cache write, fused
-            b = getattr(step, kind)
-            pa.cache_append(vals[f"k_new_{kind}"], vals[f"v_new_{kind}"], kc, vc, m["bt"], m["cu"],
-                            m["ctx"], b.max_q, m["slots"])
+        for kind in meta:  # slot mapping + cache write, fused
+            b, m = getattr(step, kind), io[kind]
+            pa.cache_append(m["kn"], m["vn"], kc, vc, m["bt"], m["cu"], m["ctx"], b.max_q,
+                            meta[kind]["slots"])
             n += 1
         if d is not None:
             if ev is not None:
                 ev[0].record(stream)
-            md = meta["decode"]
+            md = io["decode"]
             if share:
-                pa.decode_shared_prefix(out_dec, q_in["decode"], kc, vc, md["bt"], md["ctx"],
+                pa.decode_shared_prefix(io["out"]["decode"], md["q"], kc, vc, md["bt"], md["ctx"],
                                         d.max_ctx, md["pblocks"], plen, md["sharers"],
                                         step.scale, ws_dec)
                 n += 4  # plan, shared prefix, attend, merge
             else:
-                pa.decode(out_dec, q_in["decode"], kc, vc, md["bt"], md["ctx"], d.max_ctx,
+                pa.decode(io["out"]["decode"], md["q"], kc, vc, md["bt"], md["ctx"], d.max_ctx,
                           step.scale, ws_dec)
                 n += 3  # plan, attend, merge
             if ev is not None:
@@ -287,9 +295,9 @@ def run_ours(args, rank, world, local_rank):
         if p is not None:
             if ev is not None:
                 ev[2].record(stream)
-            pa.prefill_chunk(out_pre, q_in["prefill"], kc, vc, meta["prefill"]["bt"],
-                             meta["prefill"]["cu"], meta["prefill"]["ctx"], p.max_q, p.max_ctx,
-                             step.scale, ws_pre)
+            mp = io["prefill"]
+            pa.prefill_chunk(io["out"]["prefill"], mp["q"], kc, vc, mp["bt"], mp["cu"], mp["ctx"],
+                             p.max_q, p.max_ctx, step.scale, ws_pre)
             if ev is not None:
                 ev[3].record(stream)
             n += 1
@@ -326,42 +334,108 @@ def run_ours(args, rank, world, local_rank):
     if pa.get_status() != 0:
         raise RuntimeError("library status word set during the timed region")
 
-    # end to end: the step's inputs from pinned host memory, the outputs back to the host
-    h_in = {key: vals[key].cpu().pin_memory() for key in vals
-            if key.startswith(("q_", "k_new", "v_new"))}
-    h_meta = {kind: {n: m[n].cpu().pin_memory()
-                     for n in ("bt", "ctx", "cu", "pblocks", "sharers") if n in m}
-              for kind, m in meta.items()}
-    outs = ([out_dec] if d is not None else []) + ([out_pre] if p is not None else [])
-    h_outs = [torch.empty(o.shape, dtype=tdt).pin_memory() for o in outs]
-    d_in = {key: torch.empty_like(vals[key]) for key in h_in}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    h2d += sum(t.numel() * t.element_size() for m in h_meta.values() for t in m.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_outs)
+    # end to end: every step's inputs copied from pinned host memory and its outputs copied
+    # back, through a copy stream, with two sets of device buffers so that step i+1's
+    # inputs and step i-1's outputs move while step i computes (a serving loop's overlap)
+    in_names = {kind: [n for n in ("q", "kn", "vn", "bt", "ctx", "cu", "pblocks", "sharers")
+                       if n in resident_io[kind]] for kind in meta}
+    out_kinds = [kk for kk in ("decode", "prefill") if resident_io["out"][kk] is not None]
+
+    def packed(tensors, device, pin):
+        """One byte buffer holding every tensor at a 256-byte-aligned offset, and views of
+        it with the tensors' shapes and dtypes (so that one copy moves them all)."""
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for o, t in zip(offs, tensors)]
+        return buf, views
+
+    in_list = [(kind, n) for kind in in_names for n in in_names[kind]]
+    in_src = [resident_io[kind][n] for kind, n in in_list]
+    h_buf, h_views = packed(in_src, "cpu", True)
+    for v, t in zip(h_views, in_src):
+        v.copy_(t.cpu())
+    h_in = {kind: {} for kind in in_names}
+    for (kind, n), v in zip(in_list, h_views):
+        h_in[kind][n] = v
+    out_src = [resident_io["out"][kk] for kk in out_kinds]
+    d_io, d_bufs, d_outbufs, h_outbufs = [], [], [], []
+    for _ in range(2):
+        dbuf, dviews = packed(in_src, dev, False)
+        io = {kind: {} for kind in in_names}
+        for (kind, n), v in zip(in_list, dviews):
+            io[kind][n] = v
+        obuf, oviews = packed(out_src, dev, False)
+        io["out"] = {"decode": None, "prefill": None}
+        for kk, v in zip(out_kinds, oviews):
+            io["out"][kk] = v
+        d_io.append(io)
+        d_bufs.append(dbuf)
+        d_outbufs.append(obuf)
+        h_outbufs.append(packed(out_src, "cpu", True)[0])
+    h2d = sum(t.numel() * t.element_size() for h in h_in.values() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_src)
     ke = max(1, min(k, args.e2e_steps))
-    saved = dict(vals), dict(q_in)
-    for key, t in d_in.items():  # the e2e steps read their inputs from the copies
-        if key.startswith("q_"):
-            q_in[key[2:]] = t
-        else:
-            vals[key] = t
+    copy_stream = torch.cuda.Stream(dev)
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    drained = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def h2d_step(bi):
+        with torch.cuda.stream(copy_stream):
+            d_bufs[bi].copy_(h_buf, non_blocking=True)
+            ready[bi].record(copy_stream)
+
+    # the step's launches captured once per buffer set and replayed every step (inputs
+    # are read from the buffers at replay time), so that the host keeps ahead of short steps
+    graphs = []
+    if not args.no_graphs:
+        for bi in range(2):
+            d_bufs[bi].copy_(h_buf)
+            one_step(io=d_io[bi])  # the library's one-time set-up happens outside capture
+        torch.cuda.synchronize(dev)
+        for bi in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                one_step(io=d_io[bi])
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+        if pa.get_status() != 0:
+            raise RuntimeError("library status word set while capturing the step")
     barrier()
     e0, e1 = mk(), mk()
-    e0.record(stream)
-    for _ in range(ke):
-        for key, t in h_in.items():
-            d_in[key].copy_(t, non_blocking=True)
-        for kind, m in h_meta.items():
-            for n, t in m.items():
-                meta[kind][n].copy_(t, non_blocking=True)
-        one_step()
-        for ho, o in zip(h_outs, outs):
-            ho.copy_(o, non_blocking=True)
-    e1.record(stream)
+    e0.record(copy_stream)
+    for i in range(min(2, ke)):
+        h2d_step(i)
+    for i in range(ke):
+        bi = i % 2
+        stream.wait_event(ready[bi])
+        if i >= 2:
+            stream.wait_event(drained[bi])  # step i-2's outputs have left this buffer
+        if graphs:
+            graphs[bi].replay()
+        else:
+            one_step(io=d_io[bi])
+        done[bi].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(done[bi])
+            h_outbufs[bi].copy_(d_outbufs[bi], non_blocking=True)
+            drained[bi].record(copy_stream)
+        if i + 2 < ke:
+            h2d_step(bi)  # after this buffer's outputs left, on the same copy stream
+    e1.record(copy_stream)
     barrier()
+    torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / ke
-    vals.update(saved[0])
-    q_in.update(saved[1])
+    e2e_how = ("per step: one packed host-to-device copy of the inputs and one device-to-host "
+               "copy of the outputs on a copy stream, overlapping the neighbouring steps' "
+               "compute (two buffer sets); the step's launches " +
+               ("replayed from a CUDA graph" if graphs else "issued from the host"))
 
     step_ms = total_ms / k
     step_ms, dec_ms, pre_ms, e2e_ms = slowest_over_ranks([step_ms, dec_ms, pre_ms, e2e_ms], world,
@@ -414,7 +488,8 @@ def run_ours(args, rank, world, local_rank):
             "hbm_frac_of_measured": round(kvb / (step_ms * 1e-3) / 1e9 / peak, 4),
             "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 5), "steps": ke},
+                    "ms_per_step": round(e2e_ms, 5), "steps": ke,
+                    "how": e2e_how},
             "roofline": {"bound": "hbm",
                          "kernel": ("pa_decode_shared_prefix (plan + shared prefix + attend + "
                                     "merge)" if share else "pa_decode (plan + attend + merge)"),
@@ -433,7 +508,8 @@ def run_ours(args, rank, world, local_rank):
             "value": round(world * flops / (step_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 5), "steps": ke},
+                    "ms_per_step": round(e2e_ms, 5), "steps": ke,
+                    "how": e2e_how},
             "roofline": dict(pre, bound="tensor", kernel="pa_prefill_chunk",
                              traffic=recorded_traffic(args.workload)),
         })
@@ -747,6 +823,9 @@ def main():
                     help="step: the hot path over --workload; swap: pa_swap_blocks bandwidth; "
                          "blockmgr: host block-manager time per decode step")
     ap.add_argument("--swap-blocks", type=int, default=8192)
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="issue the end-to-end steps' launches from the host instead of "
+                         "replaying a captured CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
