@@ -38,6 +38,7 @@ import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; KV tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context; the roofline uses the measured copy)
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_53_gb300", "csrc", "pa_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
@@ -486,6 +487,7 @@ def run_ours(args, rank, world, local_rank):
             "value": round(world * kvb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),
             "hbm_frac_of_measured": round(kvb / (step_ms * 1e-3) / 1e9 / peak, 4),
+            "hbm_frac_of_nominal": round(kvb / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
             "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5), "steps": ke,
@@ -664,6 +666,10 @@ def _oracle_worker(payload):
     return time.perf_counter() - t, int(ctx.astype(np.int64).sum())
 
 
+def _payload_tokens(payload) -> int:
+    return int(payload[4].astype(np.int64).sum())
+
+
 def _oracle_payload(step: W.Step, seqs, gen):
     """The listed sequences of the workload with a pool of just their blocks (random
     values, same shapes and lengths), tables renumbered into that pool."""
@@ -737,6 +743,16 @@ class OraclePool:
         self.pool.map(_oracle_worker, payloads, chunksize=1)
         return time.perf_counter() - t
 
+    @staticmethod
+    def time_single(payloads):
+        """Wall time of the payloads run one after another by a single spawned
+        single-threaded worker."""
+        pool = OraclePool(1)
+        try:
+            return pool.time(payloads)
+        finally:
+            pool.close()
+
     def close(self):
         self.pool.close()
         self.pool.join()
@@ -758,10 +774,17 @@ def cpu_baseline(step: W.Step, budget_s: float):
     pool = OraclePool(workers)
     try:
         wall = pool.time(payloads)
+        # one worker alone on a slice of the same sample (about the same per-core budget)
+        one = payloads[:1]
+        one_bytes = sum(_payload_tokens(q) for q in one) * 2 * step.shape.num_kv_heads * \
+            step.shape.head_dim * step.shape.elem_bytes
+        t1 = OraclePool.time_single(one)
     finally:
         pool.close()
     return {"value": round(kvb / wall / 1e9, 4), "unit": "GB/s", "cores": workers,
-            "kind": "oracle", "sample": desc, "seconds": round(wall, 2)}
+            "kind": "oracle", "sample": desc, "seconds": round(wall, 2),
+            "single_thread": {"value": round(one_bytes / t1 / 1e9, 4), "unit": "GB/s",
+                              "seconds": round(t1, 2), "sample": "one worker's share"}}
 
 
 def run_reference(args, world):
