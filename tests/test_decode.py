@@ -140,6 +140,15 @@ def test_decode_native_output(pa, dtype):
     _full_check(pa, step, out_dtype=W._torch_dtype(dtype))
 
 
+@pytest.mark.parametrize("n,hi,dtype", [(3000, 300, "bf16"), (20000, 9, "f16"), (1500, 40, "f32")])
+def test_decode_many_sequences(pa, n, hi, dtype):
+    """More sequences than the plan kernel has threads (several per thread), short
+    contexts: tens of thousands of single-partition units and their direct outputs."""
+    ctx = np.random.default_rng(n).integers(1, hi, size=n, endpoint=True)
+    step = W.decode_step("many", W.Shape(16, 4, 64, 16, dtype), ctx, seed=n)
+    _full_check(pa, step)
+
+
 def test_decode_many_partitions_one_sequence(pa):
     """One sequence far longer than the partition size: dozens of partials merged."""
     step = W.decode_step("long1", W.Shape(32, 8, 128, 16, "bf16"), [65536 + 7], seed=13)

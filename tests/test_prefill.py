@@ -58,6 +58,16 @@ def test_prefill_shapes(pa, dtype, d, bs, h_q, h_kv):
     _check(pa, step)
 
 
+def test_prefill_many_sequences(pa):
+    """More sequences than the plan kernel has threads: 1,500 chunks of 1 to 6 tokens over
+    contexts of up to 200 tokens (one work item each per KV head)."""
+    rng = np.random.default_rng(37)
+    q = rng.integers(1, 6, size=1500, endpoint=True)
+    ctx = q + rng.integers(0, 200 - 6, size=1500, endpoint=True)
+    step = W.prefill_step("pmany", W.Shape(16, 4, 64, 16, "bf16"), ctx, q, seed=37)
+    _check(pa, step)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_prefill_native_output(pa, dtype):
     step = W.prefill_step("pn", W.Shape(32, 8, 128, 32, dtype), [512, 700], [512, 100], seed=33)

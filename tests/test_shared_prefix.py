@@ -90,6 +90,16 @@ def test_prefix_lengths(pa, prefix):
     _check(pa, step)
 
 
+def test_many_sequences_and_sharers(pa):
+    """1,200 sequences (more than the plan kernel has threads), 1,000 of them on one
+    prefix: sharer flags and reserved partial slots over many sequences per thread."""
+    rng = np.random.default_rng(38)
+    step = W.shared_prefix_step("spmany", W.Shape(32, 8, 64, 16, "bf16"), 512,
+                                rng.integers(1, 40, size=1000), rng.integers(1, 600, size=200),
+                                seed=38)
+    _check(pa, step)
+
+
 def test_only_sharers_ending_at_the_prefix(pa):
     """A sharer with no context of its own gets the prefix's attention alone (the merge
     normalises its single partial)."""
