@@ -285,63 +285,68 @@ __global__ void __launch_bounds__(384, 1)
       tc::fence_after_sync();
       const int kp0 = kv_begin + j * BN;
       const bool full = kp0 + BN <= kv_end;
-      // row maximum; on whole tiles with a positive scale the raw scores are compared
-      // and the maximum scaled once
-      const bool raw = full && sc > 0.f;
+      // row maximum over the visible positions, the whole row's scores loaded behind one
+      // wait; on whole tiles with a positive scale the raw scores are compared and the
+      // maximum scaled once
       float mx = kNegInf;
+      {
+        static_assert(BN == 128, "a 128-column row");
+        float c[4][32];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        float a[32], bq[32];
-        tc::tmem_ld32(tS + c0, a);
-        tc::tmem_ld32(tS + c0 + 32, bq);
+        for (int k = 0; k < 4; ++k) tc::tmem_ld32(tS + 32 * k, c[k]);
         tc::tmem_wait_ld();
-        if (raw) {
-          float r0 = a[0], r1 = a[1], r2 = bq[0], r3 = bq[1];
+        if (full && sc > 0.f) {
+          float rm[4];
 #pragma unroll
-          for (int i = 2; i < 32; i += 2) {
-            r0 = fmaxf(r0, a[i]);
-            r1 = fmaxf(r1, a[i + 1]);
-            r2 = fmaxf(r2, bq[i]);
-            r3 = fmaxf(r3, bq[i + 1]);
+          for (int k = 0; k < 4; ++k) {
+            rm[k] = c[k][0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) rm[k] = fmaxf(rm[k], c[k][i]);
           }
-          mx = fmaxf(mx, fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)));
-        } else if (full) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(a[i] * sc, bq[i] * sc));
+          mx = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3])) * sc;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            mx = fmaxf(mx, kp0 + c0 + i < kv_end ? a[i] * sc : kNegInf);
-            mx = fmaxf(mx, kp0 + c0 + 32 + i < kv_end ? bq[i] * sc : kNegInf);
-          }
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              mx = fmaxf(mx, kp0 + 32 * k + i < kv_end ? c[k][i] * sc : kNegInf);
         }
       }
-      if (raw) mx *= sc;
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
+      // P = 2^(scale * S - m) as hi + lo 16-bit terms over S's own columns; the next 32
+      // columns load while these are exponentiated
       float sum = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float a[32];
-        tc::tmem_ld32(tS + c0, a);
+      {
+        float buf[2][32];
+        tc::tmem_ld32(tS, buf[0]);
         tc::tmem_wait_ld();
-        if (full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
-        } else {
+        for (int k = 0; k < BN / 32; ++k) {
+          float (&a)[32] = buf[k & 1];
+          if (k + 1 < BN / 32) tc::tmem_ld32(tS + 32 * (k + 1), buf[(k + 1) & 1]);
+          const int c0 = 32 * k;
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
+            for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
+          }
+          uint32_t hi[16], lo[16];
+          float s2[2] = {0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            s2[i & 1] += a[2 * i] + a[2 * i + 1];
+            hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+          }
+          sum += s2[0] + s2[1];
+          tc::tmem_st16(tS + c0, hi);
+          tc::tmem_st16(tS + c0 + 16, lo);
+          if (k + 1 < BN / 32) tc::tmem_wait_ld();
         }
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sum += a[2 * i] + a[2 * i + 1];
-          hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
-        }
-        tc::tmem_st16(tS + c0, hi);
-        tc::tmem_st16(tS + c0 + 16, lo);
       }
       l = l * alpha + sum;
       if (j >= 1 && __any_sync(~0u, need)) {
