@@ -6,7 +6,8 @@
 //                that about kTargetUnits (partition, KV head) units exist, and writes the
 //                partition list sorted largest first (longest-processing-time order, so
 //                the dynamic scheduler below ends with the smallest units).  It also
-//                zeroes the outputs of empty contexts.
+//                zeroes the outputs of empty contexts and lists the sequences whose
+//                partials need merging.
 //   2. attend -- a persistent kernel, one CTA per SM.  Each CTA holds kPairs pairs of
 //                warps; in a pair a producer warp grabs units from a global counter,
 //                reads the unit's block-table entries, and streams every (block, KV
@@ -15,8 +16,8 @@
 //                m16n8k16, the query group padded to 16 rows) with an online softmax.
 //                A unit covering a whole context writes the normalised output; the
 //                others write an fp32 partial (running max, sum, unnormalised output).
-//   3. merge  -- one warp per (sequence, query head) with more than one partition
-//                merges its partials by log-sum-exp rescaling.  (Merging inside the attention
+//   3. merge  -- one warp per (sequence, query head) of a listed sequence merges its
+//                partials by log-sum-exp rescaling.  (Merging inside the attention
 //                kernel, by whichever warp finished last, stalled that warp's pipeline
 //                on a device-wide fence and an atomic round trip per partition, which
 //                cost more than this launch.)
@@ -68,7 +69,20 @@ __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c
 // ----------------------------------------------------------------------------------
 // 1. plan
 // ----------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ context_lens,
+
+// Claims one slot of counters[key] for every lane with key >= 0, with one shared-memory
+// atomic per distinct key in the warp; the lanes of a key take consecutive slots in lane
+// order.  Returns the lane's slot (meaningless for key < 0).  All 32 lanes must call it.
+__device__ __forceinline__ int warp_claim(int* counters, int key, int lane) {
+  const unsigned grp = __match_any_sync(~0u, key);
+  const int leader = __ffs(grp) - 1;
+  int base = 0;
+  if (key >= 0 && lane == leader) base = atomicAdd(counters + key, __popc(grp));
+  base = __shfl_sync(~0u, base, leader);
+  return base + __popc(grp & ((1u << lane) - 1));
+}
+
+__global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __restrict__ context_lens,
                                                            int num_seqs, int ctx_cap,
                                                            int num_kv_heads, int block_size,
                                                            DecodeWorkspace ws, int32_t* status,
@@ -79,7 +93,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   __shared__ long long s_sum[32];
   __shared__ int s_off[32];
   __shared__ int s_hist[kMaxPartBlocks + 2];
-  __shared__ int s_psz, s_total, s_units;
+  __shared__ int s_psz, s_total, s_units, s_nmerge;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
   const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
@@ -117,31 +131,50 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
   if (lane == 0) s_sum[wid] = sum;
   for (int i = tid; i < kMaxPartBlocks + 2; i += blockDim.x) s_hist[i] = 0;
+  if (tid == 0) s_nmerge = 0;
   __syncthreads();
-  if (tid == 0) {
-    long long total = 0;
-    for (int w = 0; w < nwarps; ++w) total += s_sum[w];
-    long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
-    want = (want + block_size - 1) / block_size * block_size;
-    want = max(want, (long long)kMinPartBlocks * block_size);
-    want = min(want, (long long)kMaxPartBlocks * block_size);
-    s_psz = (int)want;
+  if (wid == 0) {
+    long long total = lane < nwarps ? s_sum[lane] : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(~0u, total, o);
+    if (lane == 0) {
+      long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
+      want = (want + block_size - 1) / block_size * block_size;
+      want = max(want, (long long)kMinPartBlocks * block_size);
+      want = min(want, (long long)kMaxPartBlocks * block_size);
+      s_psz = (int)want;
+    }
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
   auto suffix_of = [&](int b) { return max(0, clamp_ctx(context_lens[b], ctx_cap) - start_of(b)); };
 
-  int local = 0;
-  for (int b = b0; b < b1; ++b) {
-    const int c = suffix_of(b);
-    const int np = (c + psz - 1) / psz;
-    local += np + reserved_of(b);
-    if (np > 0) {
-      const int tail = c - (np - 1) * psz;
-      atomicAdd(&s_hist[(tail + block_size - 1) / block_size], 1);
-      if (np > 1) atomicAdd(&s_hist[bpp], np - 1);
+  // Counting pass.  Every lane runs `per` iterations (so that whole warps meet in the
+  // shuffles and matches), and shared counters are bumped once per warp and distinct key.
+  auto tail_bucket = [&](int c, int np) {
+    return np > 0 ? (c - (np - 1) * psz + block_size - 1) / block_size : -1;
+  };
+  int local = 0, full = 0;
+  for (int i = 0; i < per; ++i) {
+    const int b = b0 + i;
+    int c = 0, np = 0, rs = 0;
+    if (b < b1) {
+      c = suffix_of(b);
+      np = (c + psz - 1) / psz;
+      rs = reserved_of(b);
     }
+    local += np + rs;
+    // several partials, or any for a shared prefix: the merge kernel combines them (the
+    // list's order does not matter, each sequence is merged on its own)
+    const bool merge = np + rs > 1 || rs > 0;
+    const int m = warp_claim(&s_nmerge, merge ? 0 : -1, lane);
+    if (merge) ws.merge_seqs[m] = b;
+    warp_claim(s_hist, tail_bucket(c, np), lane);
+    full += np > 1 ? np - 1 : 0;
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) full += __shfl_xor_sync(~0u, full, o);
+  if (lane == 0 && full > 0) atomicAdd(&s_hist[bpp], full);
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -195,13 +228,33 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     if (lane == 31) s_units = incl;  // partitions with a K/V range of their own
   }
   __syncthreads();
+  // Placement pass: a sequence's np - 1 full partitions take consecutive slots of the
+  // largest bucket (a warp scan of the counts and one atomic per warp), its last one a
+  // slot of its own bucket.
   run = s_off[wid] + incl - local;
-  for (int b = b0; b < b1; ++b) {
-    const int c = suffix_of(b), st = start_of(b), rs = reserved_of(b);
-    const int np = (c + psz - 1) / psz;
+  for (int i = 0; i < per; ++i) {
+    const int b = b0 + i;
+    int c = 0, st = 0, rs = 0, np = 0;
+    if (b < b1) {
+      c = suffix_of(b);
+      st = start_of(b);
+      rs = reserved_of(b);
+      np = (c + psz - 1) / psz;
+    }
+    const int nfull = np > 1 ? np - 1 : 0;
+    int fincl = nfull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(~0u, fincl, o);
+      if (lane >= o) fincl += t;
+    }
+    int fbase = 0;
+    if (lane == 31 && fincl > 0) fbase = atomicAdd(&s_hist[bpp], fincl);
+    fbase = __shfl_sync(~0u, fbase, 31) + fincl - nfull;
+    const int tslot = warp_claim(s_hist, tail_bucket(c, np), lane);
     for (int p = 0; p < np; ++p) {
       const int ntok = min(psz, c - p * psz);
-      const int slot = atomicAdd(&s_hist[(ntok + block_size - 1) / block_size], 1);
+      const int slot = p + 1 < np ? fbase + p : tslot;
       PartRec r;
       r.b = b;
       r.p = rs + p;
@@ -219,6 +272,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     ws.header[1] = s_units * num_kv_heads;
     ws.header[2] = psz;
     ws.header[3] = s_total;
+    ws.header[4] = s_nmerge;
   }
 }
 
@@ -254,52 +308,94 @@ __device__ __forceinline__ void combine_ml(float& m, float& l, float m2, float l
 }
 
 constexpr int kMaxGroup = 16;
+// Sequences with up to this many partitions are merged with one round of loads (D = 64;
+// six for D = 128, within the merge kernel's 64 registers a thread).
+constexpr int kMergeOneRound = 8;
+// Merge grid: CTAs of 256 threads per SM (at most 64 registers a thread, so that four
+// fit in the register file).
+constexpr int kMergeCtasPerSm = 4;
 
 // Merges the partials of one (sequence, query head):
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p with M = max_p m_p.  Run by one
-// warp; each lane owns D/32 consecutive columns.  Two dependent rounds of loads: the
-// (max, sum) of every partition, then every partial output row, all in flight together.
-// The partials were written by the previous kernel and are read through L2.
+// warp; each lane owns D/32 consecutive columns.  Up to kMergeOneRound partitions, every
+// (max, sum) pair and partial output row is loaded in one round; beyond that, two
+// dependent rounds: the (max, sum) of every partition, then every partial output row, all
+// in flight together.  The partials were written by the previous kernel and are read
+// through L2.
+// Loads C (4 or 2) consecutive floats through L2.
+template <int C>
+__device__ __forceinline__ void ldcg_vec(const float* ptr, float* dst) {
+  if constexpr (C == 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(ptr));
+    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+  } else {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(ptr));
+    dst[0] = v.x; dst[1] = v.y;
+  }
+}
+
 template <int D, typename TO>
 __device__ __forceinline__ void merge_row(const DecodeParams& p, int b, int hq, int ps, int np,
                                           TO* out, int lane) {
   constexpr int C = D / 32;
+  constexpr int R = C == 4 ? 6 : kMergeOneRound;
   const size_t hs = (size_t)p.num_q_heads;
   const float2* ml = p.ws.part_ml + (size_t)ps * hs + hq;  // stride hs per partition
-  float M = kNegInf, L = 0.f, m_own = kNegInf;
-  for (int i0 = 0; i0 < np; i0 += 32) {
-    const int i = i0 + lane;
-    if (i < np) {
-      const float2 v = __ldcg(ml + i * hs);
-      if (i0 == 0) m_own = v.x;
-      combine_ml(M, L, v.x, v.y);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float m2 = __shfl_xor_sync(~0u, M, o);
-    const float l2 = __shfl_xor_sync(~0u, L, o);
-    combine_ml(M, L, m2, l2);
-  }
+  const float* src = p.ws.part_acc + ((size_t)ps * hs + hq) * D + lane * C;
   float acc[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) acc[c] = 0.f;
-  const float* src = p.ws.part_acc + ((size_t)ps * hs + hq) * D + lane * C;
-  for (int i0 = 0; i0 < np; i0 += 32) {
-    const int i = i0 + lane;
-    float w = 0.f;
-    if (i < np) w = fast_exp2((i0 == 0 ? m_own : __ldcg(ml + i * hs).x) - M);
-    const int n = min(32, np - i0);
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(~0u, w, j);
-      const float* row = src + (size_t)(i0 + j) * hs * D;
-      if constexpr (C == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(row));
-        acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
-      } else {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(row));
-        acc[0] += wj * v.x; acc[1] += wj * v.y;
+  float M = kNegInf, L = 0.f;
+  if (np <= R) {
+    float2 mv[R];
+    float av[R][C];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (i < np) {
+        mv[i] = __ldcg(ml + i * hs);
+        ldcg_vec<C>(src + (size_t)i * hs * D, av[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (i < np) M = fmaxf(M, mv[i].x);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (i < np) {
+        const float w = fast_exp2(mv[i].x - M);
+        L += w * mv[i].y;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] += w * av[i][c];
+      }
+    }
+  } else {
+    float m_own = kNegInf;
+    for (int i0 = 0; i0 < np; i0 += 32) {
+      const int i = i0 + lane;
+      if (i < np) {
+        const float2 v = __ldcg(ml + i * hs);
+        if (i0 == 0) m_own = v.x;
+        combine_ml(M, L, v.x, v.y);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(~0u, M, o);
+      const float l2 = __shfl_xor_sync(~0u, L, o);
+      combine_ml(M, L, m2, l2);
+    }
+    for (int i0 = 0; i0 < np; i0 += 32) {
+      const int i = i0 + lane;
+      float w = 0.f;
+      if (i < np) w = fast_exp2((i0 == 0 ? m_own : __ldcg(ml + i * hs).x) - M);
+      const int n = min(32, np - i0);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float wj = __shfl_sync(~0u, w, j);
+        float v[C];
+        ldcg_vec<C>(src + (size_t)(i0 + j) * hs * D, v);
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] += wj * v[c];
       }
     }
   }
@@ -309,28 +405,45 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, int b, int hq, 
   for (int c = 0; c < C; c += 2) store2(o + c, acc[c] * inv, acc[c + 1] * inv);
 }
 
-// 3. merge: one warp per (sequence, query head) of a sequence with several partitions.
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, int head_dim) {
+// 3. merge: one warp per (sequence, query head) of a sequence on the plan's merge list,
+// in a grid that stays resident beside the attention kernel's last CTAs (warps loop when
+// the list has more rows than the grid has warps).
+template <int D, typename TO>
+__global__ void __launch_bounds__(256, kMergeCtasPerSm) decode_merge_kernel(const DecodeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int hs = p.num_q_heads;
+  int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // The merge list and partition table come from the plan kernel, which finished before
+  // the attention kernel passed its own dependency wait, and so before this grid was
+  // launched: a warp's first row is looked up (through L2) ahead of the wait, off the path
+  // that starts when the attention kernel ends.
+  const int rows = __ldcg(p.ws.header + 4) * hs;
+  int b = 0, ps = 0, np = 0;
+  if (r < rows) {
+    b = __ldcg(p.ws.merge_seqs + r / hs);
+    ps = __ldcg(p.ws.part_start + b);
+    np = __ldcg(p.ws.part_start + b + 1) - ps;
+  }
   griddep_wait();  // every partial of the attention kernel is written
   griddep_launch_dependents();
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= p.num_seqs * p.num_q_heads) return;
-  const int b = w / p.num_q_heads, hq = w - b * p.num_q_heads;
-  const int ps = p.ws.part_start[b];
-  const int np = p.ws.part_start[b + 1] - ps;
-  // one partition: written by the attention kernel (or zeroed by the plan), unless the
-  // sequence reads a shared prefix, whose partials always go through the merge
-  if (np <= 1 && !(p.ws.seq_flags != nullptr && p.ws.seq_flags[b])) return;
-  if (head_dim == 128) {
-    if (p.out_bytes == 4) merge_row<128, float>(p, b, hq, ps, np, static_cast<float*>(p.out), lane);
-    else if (p.out_bf16) merge_row<128, __nv_bfloat16>(p, b, hq, ps, np, static_cast<__nv_bfloat16*>(p.out), lane);
-    else merge_row<128, __half>(p, b, hq, ps, np, static_cast<__half*>(p.out), lane);
-  } else {
-    if (p.out_bytes == 4) merge_row<64, float>(p, b, hq, ps, np, static_cast<float*>(p.out), lane);
-    else if (p.out_bf16) merge_row<64, __nv_bfloat16>(p, b, hq, ps, np, static_cast<__nv_bfloat16*>(p.out), lane);
-    else merge_row<64, __half>(p, b, hq, ps, np, static_cast<__half*>(p.out), lane);
+  while (r < rows) {
+    merge_row<D, TO>(p, b, r - (r / hs) * hs, ps, np, static_cast<TO*>(p.out), lane);
+    r += nw;
+    if (r < rows) {
+      b = __ldcg(p.ws.merge_seqs + r / hs);
+      ps = __ldcg(p.ws.part_start + b);
+      np = __ldcg(p.ws.part_start + b + 1) - ps;
+    }
   }
+}
+
+using MergeKernel = void (*)(DecodeParams);
+template <int D>
+MergeKernel merge_kernel_for(pa_dtype out) {
+  if (out == PA_F32) return decode_merge_kernel<D, float>;
+  if (out == PA_BF16) return decode_merge_kernel<D, __nv_bfloat16>;
+  return decode_merge_kernel<D, __half>;
 }
 
 // ----------------------------------------------------------------------------------
@@ -839,7 +952,7 @@ size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_s
 
 namespace {
 struct WsLayout {
-  size_t header, part_start, seq_flags, units, part_ml, part_acc, total;
+  size_t header, part_start, seq_flags, merge_seqs, units, part_ml, part_acc, total;
 };
 WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
                        int block_size, long long extra_slots) {
@@ -849,7 +962,8 @@ WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head
   l.header = 0;
   l.part_start = 256;
   l.seq_flags = align_up(l.part_start + sizeof(int) * (num_seqs + 1), 256);
-  l.units = align_up(l.seq_flags + (extra_slots > 0 ? sizeof(int) * num_seqs : 0), 256);
+  l.merge_seqs = align_up(l.seq_flags + (extra_slots > 0 ? sizeof(int) * num_seqs : 0), 256);
+  l.units = align_up(l.merge_seqs + sizeof(int) * num_seqs, 256);
   l.part_ml = align_up(l.units + sizeof(PartRec) * parts, 256);
   l.part_acc = align_up(l.part_ml + sizeof(float2) * slots * num_q_heads, 256);
   l.total = align_up(l.part_acc + sizeof(float) * slots * num_q_heads * head_dim, 256);
@@ -874,6 +988,7 @@ DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads, 
   w.header = reinterpret_cast<int*>(b + l.header);
   w.part_start = reinterpret_cast<int*>(b + l.part_start);
   w.seq_flags = extra_slots > 0 ? reinterpret_cast<int*>(b + l.seq_flags) : nullptr;
+  w.merge_seqs = reinterpret_cast<int*>(b + l.merge_seqs);
   w.parts = reinterpret_cast<PartRec*>(b + l.units);
   w.part_ml = reinterpret_cast<float2*>(b + l.part_ml);
   w.part_acc = reinterpret_cast<float*>(b + l.part_acc);
@@ -907,7 +1022,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int out_row_vec16 =
       (int)((size_t)a.num_q_heads * a.head_dim * dtype_bytes(a.out_dtype) / 16);
 
-  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, a.context_lens,
+  // one CTA; a thread per sequence up to 1,024 threads (fewer warps meet in its barriers)
+  const int plan_threads = std::min(1024, std::max(32, (a.num_seqs + 31) / 32 * 32));
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(plan_threads), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
                              static_cast<int4*>(a.out), out_row_vec16, a.prefix);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
@@ -949,8 +1066,14 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     rc = launch_mma_dispatch<__half>(a, p, stream);
   }
   if (rc != PA_OK) return rc;
-  const int warps = a.num_seqs * a.num_q_heads;
-  e = launch_pdl(decode_merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, stream, p, a.head_dim);
+  // rows to merge are known only on the device: at most every (sequence, query head),
+  // in a grid of up to kMergeCtasPerSm CTAs per SM
+  const long long warps = (long long)a.num_seqs * a.num_q_heads;
+  const int merge_ctas = (int)std::min<long long>((warps + 7) / 8,
+                                                  (long long)sm_count() * kMergeCtasPerSm);
+  const MergeKernel merge =
+      a.head_dim == 128 ? merge_kernel_for<128>(a.out_dtype) : merge_kernel_for<64>(a.out_dtype);
+  e = launch_pdl(merge, dim3(std::max(1, merge_ctas)), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (merge): %s", cudaGetErrorString(e));
   return PA_OK;
 }

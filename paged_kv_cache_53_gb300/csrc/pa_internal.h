@@ -96,9 +96,11 @@ struct PartRec {
 };
 
 struct DecodeWorkspace {
-  int* header;        // [0] unit counter, [1] units, [2] part_tokens, [3] partitions
+  int* header;        // [0] unit counter, [1] units, [2] part_tokens, [3] partitions,
+                      // [4] sequences to merge
   int* part_start;    // [num_seqs + 1] first partition index of each sequence
   int* seq_flags;     // [num_seqs] 1 for a sequence reading the shared prefix (or null)
+  int* merge_seqs;    // [num_seqs] the sequences whose partials the merge combines
   PartRec* parts;     // [max_parts] partitions, largest first
   float2* part_ml;    // [max_parts * num_q_heads] (running max in log2 units, sum)
   float* part_acc;    // [max_parts * num_q_heads * head_dim] unnormalised outputs
