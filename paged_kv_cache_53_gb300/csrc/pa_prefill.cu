@@ -24,7 +24,7 @@
 //              keep the running max (moved only when it grows by more than 2^8,
 //              rescaling O in TMEM then) and sum, write P as fp16 over S's own TMEM
 //              columns; at the end normalise O and store.  While the tensor core works,
-//              each warpgroup also converts half of the next K/V tile's V from bf16 to
+//              each warpgroup also converts half of the next step's V tile from bf16 to
 //              fp16 in place (exact below 65520 in magnitude; larger values are flagged)
 //              and zeroes the V rows past the context, which would otherwise meet P = 0
 //              with whatever bits they hold.  One conversion serves both query tiles.
@@ -68,18 +68,23 @@ struct PrefillCfg {
   static constexpr int kQBytes = kHalves * kQHalfBytes;
   static constexpr int kKvHalfBytes = BN * 128;        // 16 KiB
   static constexpr int kKBytes = kHalves * kKvHalfBytes;
-  static constexpr int kStageBytes = 2 * kKBytes;      // K then V
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  // separate rings for K and V tiles.  V(j+1) is converted as soon as P(j) is out, and
+  // its slot frees only when both P(j-1) V(j-1) products are done: with two V stages its
+  // load would start about one step before it is needed, less than a load's latency, and
+  // the softmax warpgroups would wait for it.  A third V stage starts the load a step
+  // earlier.
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = kKStages + 1;
   static constexpr int kBlocksPerTile = BN / BS;
   static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 softmax WGs
   static constexpr int kVThreads = 256;                // both softmax WGs convert V
   static constexpr int kTmemCols = 512;                // S/P_A | S/P_B | O_A | O_B
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_ready[S], then per
-  // query tile s_full, p_full, pv_done.  K and V of a stage have barriers of their own:
-  // K(j) is done with once S(j) has been computed, an iteration before P(j) V(j), so the
-  // next K tile can load that much earlier.
-  static constexpr int kBars = 1 + 5 * kStages + 3 * kTiles;
-  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
+  // barriers: q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], v_ready[SV], then
+  // per query tile s_full, p_full, pv_done.  K(j) is done with once S(j) has been
+  // computed, an iteration before P(j) V(j), so the next K tile loads that much earlier.
+  static constexpr int kBars = 1 + 2 * kKStages + 3 * kVStages + 3 * kTiles;
+  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes +
+                                  (size_t)(kKStages + kVStages) * kKBytes +
                                   kBars * 8 + 16;
 };
 
@@ -203,21 +208,23 @@ __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   using C = PrefillCfg<D, BS>;
-  constexpr int BN = C::BN, S = C::kStages, NT = C::kTiles;
+  constexpr int BN = C::BN, SK = C::kKStages, SV = C::kVStages, NT = C::kTiles;
+  static_assert(C::kSmem <= 232448, "shared memory per CTA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = base;                              // [tile][half][128 rows][128 B]
-  uint8_t* sKV = sQ + NT * C::kQBytes;             // [stage][K | V][half][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
+  uint8_t* sK = sQ + NT * C::kQBytes;              // [K stage][half][128 rows][128 B]
+  uint8_t* sV = sK + SK * C::kKBytes;              // [V stage][half][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 1 + S;
-  uint64_t* v_full = bars + 1 + 2 * S;
-  uint64_t* v_empty = bars + 1 + 3 * S;
-  uint64_t* v_ready = bars + 1 + 4 * S;  // V of the stage converted to fp16
-  uint64_t* s_full = bars + 1 + 5 * S;   // [tile]
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* v_ready = v_empty + SV;      // V of the stage converted to fp16
+  uint64_t* s_full = v_ready + SV;       // [tile]
   uint64_t* p_full = s_full + NT;
   uint64_t* pv_done = p_full + NT;
 
@@ -251,9 +258,11 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(q_full), 1);
-    for (int i = 0; i < S; ++i) {
+    for (int i = 0; i < SK; ++i) {
       mbar_init(smem_addr(k_full + i), 1);
       mbar_init(smem_addr(k_empty + i), 1);
+    }
+    for (int i = 0; i < SV; ++i) {
       mbar_init(smem_addr(v_full + i), 1);
       mbar_init(smem_addr(v_empty + i), 1);
       mbar_init(smem_addr(v_ready + i), C::kVThreads);
@@ -301,7 +310,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j % S;
       const int bi = j * C::kBlocksPerTile + lane;
       int id = -1;
       if (lane < C::kBlocksPerTile && bi < nblk_ctx) {
@@ -314,10 +322,11 @@ __global__ void __launch_bounds__(384, 1)
       // K of tile j, then its V, each once its slot's previous tile is done with
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
+        const int ns = kv == 0 ? SK : SV, s = j % ns;
         uint64_t* full = kv == 0 ? k_full : v_full;
         uint64_t* empty = kv == 0 ? k_empty : v_empty;
-        if (!mbar_wait(smem_addr(empty + s), ((j / S) & 1) ^ 1)) { ok = false; break; }
-        uint8_t* st = sKV + s * C::kStageBytes + kv * C::kKBytes;
+        if (!mbar_wait(smem_addr(empty + s), ((j / ns) & 1) ^ 1)) { ok = false; break; }
+        uint8_t* st = (kv == 0 ? sK : sV) + s * C::kKBytes;
         const CUtensorMap* map = kv == 0 ? &tmk : &tmv;
         if (lane == 0) mbar_arrive_expect_tx(smem_addr(full + s), C::kKBytes);
 #pragma unroll
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(384, 1)
       auto issue_s = [&](int x, int j) {
         const uint32_t tS = tmem + x * BN;
         const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
-        const uint32_t sk = smem_addr(sKV + (j % S) * C::kStageBytes);
+        const uint32_t sk = smem_addr(sK + (j % SK) * C::kKBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
@@ -361,13 +370,13 @@ __global__ void __launch_bounds__(384, 1)
       auto issue_pv = [&](int x, int j) -> bool {
         if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
         if (v_seen < j) {
-          if (!mbar_wait(smem_addr(v_ready + j % S), (j / S) & 1)) return false;
+          if (!mbar_wait(smem_addr(v_ready + j % SV), (j / SV) & 1)) return false;
           v_seen = j;
         }
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint32_t sv = smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes);
+        const uint32_t sv = smem_addr(sV + (j % SV) * C::kKBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
@@ -391,15 +400,15 @@ __global__ void __launch_bounds__(384, 1)
           if (j < tg[x].n_kv && !issue_pv(x, j)) { ok = false; break; }
           if (j + 1 < tg[x].n_kv) {
             if (!next_ready) {
-              if (!mbar_wait(smem_addr(k_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
+              if (!mbar_wait(smem_addr(k_full + (j + 1) % SK), ((j + 1) / SK) & 1)) { ok = false; break; }
               tc::fence_after_sync();
               next_ready = true;
             }
             issue_s(x, j + 1);
           }
         }
-        tc::commit(smem_addr(v_empty + j % S));                   // V(j): both PV(j) issued
-        if (j + 1 < n_kv) tc::commit(smem_addr(k_empty + (j + 1) % S));  // K(j+1): both S
+        tc::commit(smem_addr(v_empty + j % SV));                    // V(j): both PV(j) issued
+        if (j + 1 < n_kv) tc::commit(smem_addr(k_empty + (j + 1) % SK));  // K(j+1): both S
       }
       if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
@@ -420,10 +429,10 @@ __global__ void __launch_bounds__(384, 1)
     const int vt = threadIdx.x - 128;
     __half2 vmax = __floats2half2_rn(0.f, 0.f);  // largest |v| converted, per lane half
     auto convert_v = [&](int jv) -> bool {
-      const int s = jv % S;
-      if (!mbar_wait(smem_addr(v_full + s), (jv / S) & 1)) return false;
+      const int s = jv % SV;
+      if (!mbar_wait(smem_addr(v_full + s), (jv / SV) & 1)) return false;
       const int z0 = ctx - jv * BN;  // rows from z0 on lie past the context
-      uint4* sv = reinterpret_cast<uint4*>(sKV + s * C::kStageBytes + C::kKBytes);
+      uint4* sv = reinterpret_cast<uint4*>(sV + s * C::kKBytes);
       constexpr int kPer = C::kKBytes / 16 / C::kVThreads;
       uint4 v[kPer];
 #pragma unroll
@@ -453,6 +462,7 @@ __global__ void __launch_bounds__(384, 1)
       return true;
     };
     float m = kNegInf, l = 0.f;
+    // V tiles 0 and 1 before the first step, then tile j+2 after step j
     if (n_kv > 0 && !convert_v(0)) ok = false;
     for (int j = 0; j < g.n_kv && ok; ++j) {
       if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
