@@ -18,16 +18,20 @@
 //              PV_B(j), S_B(j+1), so that one tile's softmax overlaps the other tile's
 //              products.  PV runs in fp16: P rounded to fp16 has a unit roundoff of
 //              2^-11, which keeps the output within a 2e-3 absolute bound where bf16's
-//              2^-8 would not.  S = Q K^T runs in the input type.
+//              2^-8 would not.  S = Q K^T runs in the input type.  The issuing thread
+//              shares its scheduler with two busy softmax warps and gets only part of
+//              its issue slots, so it spends as few instructions per MMA as it can
+//              (descriptors advanced by constant offsets from precomputed ones).
 //   warps 4-11 two softmax warpgroups, one per query tile, one thread per row: read
 //              the row of S from TMEM into registers, apply scale and the causal mask,
 //              keep the running max (moved only when it grows by more than 2^8,
 //              rescaling O in TMEM then) and sum, write P as fp16 over S's own TMEM
-//              columns; at the end normalise O and store.  While the tensor core works,
-//              each warpgroup also converts half of the next step's V tile from bf16 to
-//              fp16 in place (exact below 65520 in magnitude; larger values are flagged)
-//              and zeroes the V rows past the context, which would otherwise meet P = 0
-//              with whatever bits they hold.  One conversion serves both query tiles.
+//              columns; at the end normalise O and store.
+//   warps 2-3, and the softmax warps not on the MMA issuer's scheduler: convert the
+//              next step's V tile from bf16 to fp16 in place (exact below 65520 in
+//              magnitude; larger values are flagged) and zero the V rows past the
+//              context, which would otherwise meet P = 0 with whatever bits they hold.
+//              One conversion serves both query tiles.
 // Tiles wholly above the diagonal are never loaded.
 #include <algorithm>
 #include <mutex>
@@ -76,8 +80,8 @@ struct PrefillCfg {
   static constexpr int kKStages = D == 128 ? 2 : 4;
   static constexpr int kVStages = kKStages + 1;
   static constexpr int kBlocksPerTile = BN / BS;
-  static constexpr int kThreads = 384;                 // producer, MMA, 2 idle, 2 softmax WGs
-  static constexpr int kVThreads = 256;                // both softmax WGs convert V
+  static constexpr int kThreads = 384;                 // producer, MMA, 2 converters, 2 softmax WGs
+  static constexpr int kVThreads = 256;                // threads converting V
   static constexpr int kTmemCols = 512;                // S/P_A | S/P_B | O_A | O_B
   // barriers: q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], v_ready[SV], then
   // per query tile s_full, p_full, pv_done.  K(j) is done with once S(j) has been
@@ -290,6 +294,50 @@ __global__ void __launch_bounds__(384, 1)
   // TMEM columns: S of tile x at x * BN (P_x is written over its first half: token t of
   // the K/V tile in column t / 2, two fp16 per column), O of tile x at NT * BN + x * D.
   bool ok = true;
+  // V of K/V tile jv: bf16 -> fp16 in place and rows past the context zeroed, by 256
+  // converting threads, each taking every 256th 16-byte piece: warps 2-3 and the six
+  // softmax warps that do not share a scheduler (warp index mod 4) with the MMA issuer
+  int vt = -1;
+  if (warp == 2 || warp == 3) {
+    vt = threadIdx.x - 64;
+  } else if (warp >= 4 && (warp & 3) != 1) {
+    const int q = warp - 4;
+    vt = 64 + 32 * (q - (q >= 2 ? 1 : 0) - (q >= 6 ? 1 : 0)) + lane;
+  }
+  __half2 vmax = __floats2half2_rn(0.f, 0.f);  // largest |v| converted, per lane half
+  auto convert_v = [&](int jv) -> bool {
+    const int s = jv % SV;
+    if (!mbar_wait(smem_addr(v_full + s), (jv / SV) & 1)) return false;
+    const int z0 = ctx - jv * BN;  // rows from z0 on lie past the context
+    uint4* sv = reinterpret_cast<uint4*>(sV + s * C::kKBytes);
+    constexpr int kPer = C::kKBytes / 16 / C::kVThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) v[u] = sv[vt + u * C::kVThreads];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      // a piece's row: rows are 128 bytes in every 64-column half (the swizzle only
+      // permutes pieces within a row); pieces past the context become zeros
+      const int i = vt + u * C::kVThreads;
+      if (z0 < BN && ((i % (C::kKvHalfBytes / 16)) >> 3) >= z0) {
+        v[u] = make_uint4(0, 0, 0, 0);
+      } else if constexpr (Fmt<T>::v == 1) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16),
+                                               __uint_as_float(w[k] & 0xffff0000u));
+          vmax = __hmax2(vmax, __habs2(hv));
+          w[k] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) sv[vt + u * C::kVThreads] = v[u];
+    tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+    mbar_arrive(smem_addr(v_ready + s));
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -353,16 +401,18 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM, BN, false, false);
       const uint32_t id_o = tc::idesc_f16(Fmt<__half>::v, C::BM, D, false, true);  // fp16 P, V
+      // descriptors of each operand's first k-step, advanced by constant offsets below
+      uint64_t dq[NT];
+#pragma unroll
+      for (int x = 0; x < NT; ++x) dq[x] = tc::smem_desc_sw128(smem_addr(sQ + x * C::kQBytes), 16, 1024);
       auto issue_s = [&](int x, int j) {
         const uint32_t tS = tmem + x * BN;
-        const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
-        const uint32_t sk = smem_addr(sK + (j % SK) * C::kKBytes);
+        const uint64_t dk = tc::smem_desc_sw128(smem_addr(sK + (j % SK) * C::kKBytes), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          const uint64_t a = tc::smem_desc_sw128(sq + (kk >> 2) * C::kQHalfBytes + koff, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(sk + (kk >> 2) * C::kKvHalfBytes + koff, 16, 1024);
-          tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
+          tc::mma_f16_ss(tS, tc::desc_advance(dq[x], (kk >> 2) * C::kQHalfBytes + koff),
+                         tc::desc_advance(dk, (kk >> 2) * C::kKvHalfBytes + koff), id_s, kk > 0);
         }
         tc::commit(smem_addr(s_full + x));
       };
@@ -376,12 +426,11 @@ __global__ void __launch_bounds__(384, 1)
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint32_t sv = smem_addr(sV + (j % SV) * C::kKBytes);
+        const uint64_t dv =
+            tc::smem_desc_sw128(smem_addr(sV + (j % SV) * C::kKBytes), C::kKvHalfBytes, 1024);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
-          tc::mma_f16_ts(tO, tP + 8 * ks, bdesc, id_o, j > 0 || ks > 0);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          tc::mma_f16_ts(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o, j > 0 || ks > 0);
         tc::commit(smem_addr(pv_done + x));
         return true;
       };
@@ -413,6 +462,14 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
     __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    for (int jv = 0; jv < n_kv && ok; ++jv)
+      if (!convert_v(jv)) ok = false;
+    if constexpr (Fmt<T>::v == 1) {
+      const float2 vm = __half22float2(vmax);
+      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) flag_status(p.status, PA_STATUS_RANGE);
+    }
+    if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp >= 4) {
     // --------------------------- softmax / epilogue (one WG per tile) ---------------------------
     const int x = (warp - 4) >> 2;                           // query tile of this warpgroup
@@ -424,46 +481,9 @@ __global__ void __launch_bounds__(384, 1)
     const int rpos = ctx0 + g.t0 + r / G;                    // position of this row's query
     const int rpos_warp = ctx0 + g.t0 + (r & ~31) / G;       // smallest position in the warp
     const float sc = p.scale_log2;
-    // V of K/V tile jv: bf16 -> fp16 in place and rows past the context zeroed, this
-    // thread taking every 256th 16-byte piece
-    const int vt = threadIdx.x - 128;
-    __half2 vmax = __floats2half2_rn(0.f, 0.f);  // largest |v| converted, per lane half
-    auto convert_v = [&](int jv) -> bool {
-      const int s = jv % SV;
-      if (!mbar_wait(smem_addr(v_full + s), (jv / SV) & 1)) return false;
-      const int z0 = ctx - jv * BN;  // rows from z0 on lie past the context
-      uint4* sv = reinterpret_cast<uint4*>(sV + s * C::kKBytes);
-      constexpr int kPer = C::kKBytes / 16 / C::kVThreads;
-      uint4 v[kPer];
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) v[u] = sv[vt + u * C::kVThreads];
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        // a piece's row: rows are 128 bytes in every 64-column half (the swizzle only
-        // permutes pieces within a row); pieces past the context become zeros
-        const int i = vt + u * C::kVThreads;
-        if (z0 < BN && ((i % (C::kKvHalfBytes / 16)) >> 3) >= z0) {
-          v[u] = make_uint4(0, 0, 0, 0);
-        } else if constexpr (Fmt<T>::v == 1) {
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __half2 hv = __floats2half2_rn(__uint_as_float(w[k] << 16),
-                                                 __uint_as_float(w[k] & 0xffff0000u));
-            vmax = __hmax2(vmax, __habs2(hv));
-            w[k] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) sv[vt + u * C::kVThreads] = v[u];
-      tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
-      mbar_arrive(smem_addr(v_ready + s));
-      return true;
-    };
     float m = kNegInf, l = 0.f;
-    // V tiles 0 and 1 before the first step, then tile j+2 after step j
-    if (n_kv > 0 && !convert_v(0)) ok = false;
+    // V tile 0 before the first step, then tile j+1 after step j
+    if (n_kv > 0 && vt >= 0 && !convert_v(0)) ok = false;
     for (int j = 0; j < g.n_kv && ok; ++j) {
       if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
@@ -539,11 +559,11 @@ __global__ void __launch_bounds__(384, 1)
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(smem_addr(p_full + x));
-      if (j + 1 < n_kv && !convert_v(j + 1)) { ok = false; break; }
+      if (j + 1 < n_kv && vt >= 0 && !convert_v(j + 1)) { ok = false; break; }
     }
     // the CTA's K/V tiles past this tile's last (the other tile reaches further) still
     // need this warpgroup's half of their conversion
-    for (int jv = g.n_kv + 1; jv < n_kv && ok; ++jv)
+    for (int jv = g.n_kv + 1; jv < n_kv && ok && vt >= 0; ++jv)
       if (!convert_v(jv)) ok = false;
     if constexpr (Fmt<T>::v == 1) {
       // a value at or above 65520 in magnitude became inf (NaN stays NaN): flag it

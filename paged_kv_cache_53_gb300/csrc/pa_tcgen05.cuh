@@ -55,6 +55,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   return d;
 }
 
+// The descriptor of an operand `bytes` further on in shared memory: the start address is
+// held in 16-byte units in the low 14 bits, which shared addresses (below 256 KiB) never
+// overflow, so the offset adds without a carry into the other fields.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulation, A and B both fp16 (fmt 0) or
 // both bf16 (fmt 1); a_mn / b_mn select MN-major operands.
 __host__ __device__ constexpr uint32_t idesc_f16(int fmt, int m, int n, bool a_mn, bool b_mn) {
