@@ -201,6 +201,22 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // Per query tile of a CTA: where it starts in the chunk and how far it reaches.
+// Packed fp32 pairs (the f32x2 arithmetic of sm_100-class SMs): one packed FMA does the
+// work of two, which matters here because every instruction of the softmax warps competes
+// with the MMA issuer for its scheduler's issue slots.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 struct TileGeom {
   int t0;       // first chunk token
   int ntok;     // chunk tokens in the tile (0: the tile lies past the chunk)
@@ -528,14 +544,19 @@ __global__ void __launch_bounds__(384, 1)
       if (need) m = mx;
       // P = 2^(scale * S - m) in fp16, tokens 32k .. 32k+31 into columns 16k .. 16k+15
       // (the scores there are already in registers)
+      // exponent t = scale * S - m (the diagonal's scores are scaled already: factor 1),
+      // two columns per packed FMA (each lane rounds as a scalar fmaf would)
+      const float f = full ? sc : 1.f;
+      const uint64_t f2x = f2(f, f), negm2 = f2(-m, -m);
       float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float e0 = fast_exp2(full ? fmaf(c[k][2 * i], sc, -m) : c[k][2 * i] - m);
-          const float e1 = fast_exp2(full ? fmaf(c[k][2 * i + 1], sc, -m) : c[k][2 * i + 1] - m);
+          float t0, t1;
+          f2_split(f2_fma(f2(c[k][2 * i], c[k][2 * i + 1]), f2x, negm2), t0, t1);
+          const float e0 = fast_exp2(t0), e1 = fast_exp2(t1);
           s2[i & 3] += e0 + e1;
           pk[i] = Mma<__half>::pack(e0, e1);
         }
