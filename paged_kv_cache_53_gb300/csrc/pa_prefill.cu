@@ -201,22 +201,6 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // Per query tile of a CTA: where it starts in the chunk and how far it reaches.
-// Packed fp32 pairs (the f32x2 arithmetic of sm_100-class SMs): one packed FMA does the
-// work of two, which matters here because every instruction of the softmax warps competes
-// with the MMA issuer for its scheduler's issue slots.
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
 struct TileGeom {
   int t0;       // first chunk token
   int ntok;     // chunk tokens in the tile (0: the tile lies past the chunk)

@@ -214,16 +214,19 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(SpFmt<T>::v, C::BM, BN, false, false);
       const uint32_t id_o = tc::idesc_f16(SpFmt<T>::v, C::BM, D, false, true);
+      // descriptors of each operand's first k-step, advanced by constant offsets (fewer
+      // instructions per MMA for a thread that shares its scheduler with softmax warps)
+      uint64_t dq[NT];
+#pragma unroll
+      for (int x = 0; x < NT; ++x) dq[x] = tc::smem_desc_sw128(smem_addr(sQ + x * C::kQBytes), 16, 1024);
       auto issue_s = [&](int x, int j) {
         const uint32_t tS = tmem + x * BN;
-        const uint32_t sq = smem_addr(sQ + x * C::kQBytes);
-        const uint32_t sk = smem_addr(sKV + (j % S) * C::kStageBytes);
+        const uint64_t dk = tc::smem_desc_sw128(smem_addr(sKV + (j % S) * C::kStageBytes), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          const uint64_t a = tc::smem_desc_sw128(sq + (kk >> 2) * C::kQHalfBytes + koff, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(sk + (kk >> 2) * C::kKvHalfBytes + koff, 16, 1024);
-          tc::mma_f16_ss(tS, a, bd, id_s, kk > 0);
+          tc::mma_f16_ss(tS, tc::desc_advance(dq[x], (kk >> 2) * C::kQHalfBytes + koff),
+                         tc::desc_advance(dk, (kk >> 2) * C::kKvHalfBytes + koff), id_s, kk > 0);
         }
         tc::commit(smem_addr(s_full + x));
       };
@@ -232,11 +235,12 @@ __global__ void __launch_bounds__(384, 1)
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint32_t sv = smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes);
+        const uint64_t dv = tc::smem_desc_sw128(
+            smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes), C::kKvHalfBytes, 1024);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
-          const uint64_t bdesc = tc::smem_desc_sw128(sv + ks * 16 * 128, C::kKvHalfBytes, 1024);
+          const uint64_t bdesc = tc::desc_advance(dv, ks * 16 * 128);
           tc::mma_f16_ts(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
           tc::mma_f16_ts(tO, tP + col + 16, bdesc, id_o, true);
         }
@@ -328,8 +332,14 @@ __global__ void __launch_bounds__(384, 1)
           if (k + 1 < BN / 32) tc::tmem_ld32(tS + 32 * (k + 1), buf[(k + 1) & 1]);
           const int c0 = 32 * k;
           if (full) {
+            const uint64_t sc2 = f2(sc, sc), negm2 = f2(-m, -m);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = fast_exp2(fmaf(a[i], sc, -m));
+            for (int i = 0; i < 16; ++i) {
+              float t0, t1;
+              f2_split(f2_fma(f2(a[2 * i], a[2 * i + 1]), sc2, negm2), t0, t1);
+              a[2 * i] = fast_exp2(t0);
+              a[2 * i + 1] = fast_exp2(t1);
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
