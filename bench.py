@@ -88,6 +88,18 @@ def prefill_useful_flops(step: W.Step) -> int:
     return 4 * sh.head_dim * sh.num_q_heads * visible
 
 
+def prefill_algorithmic_bytes(step: W.Step, out_bytes: int) -> int:
+    """Bytes a prefill call must move at least: every context position's K and V row of
+    its KV head once, the query rows in and the output rows out, the block-table entries
+    and lengths."""
+    sh, b = step.shape, step.prefill
+    ctx = b.context_lens.astype(np.int64)
+    kv = int(ctx.sum()) * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+    rows = b.num_new_tokens * sh.num_q_heads * sh.head_dim
+    tables = int(((ctx + sh.block_size - 1) // sh.block_size).sum()) * 4 + 8 * b.num_seqs
+    return kv + rows * (sh.elem_bytes + out_bytes) + tables
+
+
 def measured_peaks(kind: str = "hbm"):
     """HBM GB/s, or bf16 dense TFLOP/s (burst), from the driver's measurements."""
     key, fallback = ("hbm_gbs", FALLBACK_HBM_GBS) if kind == "hbm" else ("bf16_tflops", 1900.0)
@@ -516,6 +528,18 @@ def run_ours(args, rank, world, local_rank):
         })
         if p is not None:
             res["prefill"] = pre
+            # the step's roofline: the decode call at HBM bandwidth plus the prefill call at
+            # the slower of its tensor-core and HBM times
+            pf_bytes = prefill_algorithmic_bytes(step, out_pre.element_size())
+            t_dec = alg / (peak * 1e9)
+            t_pf = max(pre["useful_gflop"] * 1e9 / (pre["peak"] * 1e12), pf_bytes / (peak * 1e9))
+            res["step_roofline"] = {
+                "ms": round((t_dec + t_pf) * 1e3, 5), "decode_ms": round(t_dec * 1e3, 5),
+                "prefill_ms": round(t_pf * 1e3, 5), "prefill_algorithmic_bytes": pf_bytes,
+                "frac": round((t_dec + t_pf) * 1e3 / step_ms, 4),
+                "how": "decode algorithmic bytes / measured HBM GB/s + max(prefill useful "
+                       "flops / measured bf16 TFLOP/s, prefill bytes / measured HBM GB/s), "
+                       "over the measured step time"}
     else:  # a prefill-only workload: useful causal TFLOP/s against the tensor roofline
         flops = prefill_useful_flops(step)
         res.update({
