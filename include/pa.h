@@ -73,6 +73,15 @@ const char* pa_last_error_string(void);
  * the device.  Returns PA_ERR_CUDA if the device cannot be reached. */
 int pa_get_status(int32_t* status);
 
+/* Self-test of the kernels' bounded waits: launches one CTA on `stream` (cudaStream_t,
+ * may be null) that waits on a shared-memory mbarrier nothing ever arrives on, with the
+ * wait function every pipeline in this library uses, given up after `timeout_us`
+ * microseconds (1 .. 2,000,000) instead of the library's 2 s.  The kernel then sets
+ * PA_STATUS_TIMEOUT in the status word and returns: the device stays usable, and
+ * pa_get_status() reports the bit.  No other effect.  Returns PA_ERR_INVALID_ARG for a
+ * timeout out of range, PA_ERR_CUDA if the launch fails. */
+int pa_selftest_wait_timeout(int timeout_us, void* stream);
+
 /*
  * pa_slot_mapping -- physical slot of every new token of a step.
  *

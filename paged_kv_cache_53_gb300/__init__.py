@@ -52,6 +52,7 @@ _SIGNATURES = {
     "pa_version": ([], _i),
     "pa_last_error_string": ([], ctypes.c_char_p),
     "pa_get_status": ([_p], _i),
+    "pa_selftest_wait_timeout": ([_i, _p], _i),
     "pa_slot_mapping": ([_p, _p, _i, _p, _p, _i, _i, _i, _i, _p], _i),
     "pa_reshape_and_cache": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _p], _i),
@@ -267,3 +268,9 @@ def get_status() -> int:
     v = ctypes.c_int32(0)
     _check(lib().pa_get_status(ctypes.byref(v)))
     return int(v.value)
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None):
+    """Runs the bounded-wait self-test: one kernel waits on an mbarrier nothing arrives
+    on, gives up after `timeout_us` microseconds and sets STATUS_TIMEOUT."""
+    _check(lib().pa_selftest_wait_timeout(int(timeout_us), _stream(stream)))

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -156,6 +157,22 @@ int encode_query_map(CUtensorMap* map, const void* q, pa_dtype dtype, int num_to
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+namespace {
+// One thread waits on an mbarrier initialised for one arrival that never comes.
+__global__ void selftest_wait_kernel(uint64_t timeout_ns, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_addr(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait(smem_addr(&bar), 0, timeout_ns)) flag_status(status, PA_STATUS_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int32_t* status, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns, status);
+  return cudaGetLastError();
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -165,6 +182,20 @@ extern "C" {
 int pa_version(void) { return 100; }
 
 const char* pa_last_error_string(void) { return g_error; }
+
+int pa_selftest_wait_timeout(int timeout_us, void* stream) {
+  pa::clear_error();
+  if (timeout_us < 1 || timeout_us > 2000000)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_selftest_wait_timeout: timeout_us %d outside [1, 2e6]",
+                    timeout_us);
+  int32_t* st = pa::status_word();
+  if (st == nullptr) return pa::fail(PA_ERR_CUDA, "pa_selftest_wait_timeout: no usable device");
+  const cudaError_t e = pa::launch_selftest_wait((uint64_t)timeout_us * 1000ull, st,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return pa::fail(PA_ERR_CUDA, "pa_selftest_wait_timeout: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
 
 int pa_get_status(int32_t* status) {
   g_error[0] = '\0';

@@ -64,15 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if it has not
-// after kWaitTimeoutNs; the caller records the timeout and stops.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// after `timeout_ns` (kWaitTimeoutNs unless a self-test asks for less); the caller
+// records the timeout and stops.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - start > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - start > timeout_ns) return false;
   }
 }
 

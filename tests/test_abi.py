@@ -118,6 +118,13 @@ def test_get_status_without_output_pointer(lib):
     assert lib.pa_get_status(None) == 1
 
 
+@pytest.mark.parametrize("us", [0, -5, 2_000_001])
+def test_selftest_wait_rejects_timeouts_out_of_range(lib, us):
+    # checked before any device is touched
+    assert lib.pa_selftest_wait_timeout(us, None) == 1
+    assert b"timeout_us" in lib.pa_last_error_string()
+
+
 def _shared(lib, **kw):
     a = dict(out=FAKE, out_dtype=2, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxblk=64, ctx=FAKE,
              max_ctx=1024, B=4, Hq=32, Hkv=8, D=128, BS=16, NB=64, pb=FAKE, plen=512, sh=FAKE,
