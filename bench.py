@@ -247,6 +247,8 @@ def run_ours(args, rank, world, local_rank):
     pairs = torch.from_numpy(step.cow_pairs).to(dev) if step.cow_pairs is not None else None
     d, p = step.decode, step.prefill
     share = d is not None and step.shared_prefix is not None and args.share_prefix == "on"
+    # a plain decode batch takes the fused step call (cache write + decode)
+    fused_decode = d is not None and not share and args.decode_append == "on"
     if d is not None:
         out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
         if share:
@@ -286,6 +288,8 @@ def run_ours(args, rank, world, local_rank):
             pa.copy_blocks([kc], [vc], pairs)
             n += 1
         for kind in meta:  # slot mapping + cache write, fused
+            if kind == "decode" and fused_decode:
+                continue  # written by pa_decode_append below
             b, m = getattr(step, kind), io[kind]
             pa.cache_append(m["kn"], m["vn"], kc, vc, m["bt"], m["cu"], m["ctx"], b.max_q,
                             meta[kind]["slots"])
@@ -294,7 +298,12 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev[0].record(stream)
             md = io["decode"]
-            if share:
+            if fused_decode:
+                pa.decode_append(io["out"]["decode"], md["q"], md["kn"], md["vn"], kc, vc,
+                                 md["bt"], md["ctx"], d.max_ctx, step.scale, ws_dec,
+                                 slots=meta["decode"]["slots"])
+                n += 4  # cache write, plan, attend, merge
+            elif share:
                 pa.decode_shared_prefix(io["out"]["decode"], md["q"], kc, vc, md["bt"], md["ctx"],
                                         d.max_ctx, md["pblocks"], plen, md["sharers"],
                                         step.scale, ws_dec)
@@ -493,6 +502,8 @@ def run_ours(args, rank, world, local_rank):
         kv_tokens = int(d.context_lens.astype(np.int64).sum())
         peak, peak_kind = measured_peaks()
         alg = decode_algorithmic_bytes(step, out_dec.element_size(), shared=share)
+        if fused_decode:  # the call also reads the new K/V rows, writes them and the slots
+            alg += 2 * 2 * d.num_seqs * sh.num_kv_heads * sh.head_dim * sh.elem_bytes + 8 * d.num_seqs
         achieved = alg / (dec_ms * 1e-3) / 1e9
         config.update({"num_seqs": d.num_seqs, "kv_tokens_per_step": kv_tokens,
                        "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
@@ -519,7 +530,9 @@ def run_ours(args, rank, world, local_rank):
                     "how": e2e_how},
             "roofline": {"bound": "hbm",
                          "kernel": ("pa_decode_shared_prefix (plan + shared prefix + attend + "
-                                    "merge)" if share else "pa_decode (plan + attend + merge)"),
+                                    "merge)" if share else
+                                    "pa_decode_append (cache write + plan + attend + merge)"
+                                    if fused_decode else "pa_decode (plan + attend + merge)"),
                          "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": None if share else recorded_traffic(args.workload),
@@ -871,6 +884,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.NAMED), default="llama8b_gqa_decode")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--decode-append", choices=["on", "off"], default="on",
+                    help="on: a plain decode batch's cache write and decode in one call "
+                         "(pa_decode_append); off: pa_cache_append then pa_decode")
     ap.add_argument("--share-prefix", choices=["on", "off"], default="on",
                     help="workloads with a shared prefix: attend it once for all sharers "
                          "(pa_decode_shared_prefix) or per sequence (pa_decode)")

@@ -221,6 +221,33 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_append -- one decode step: write each sequence's new token into the cache,
+ * then pa_decode.
+ *
+ * Equivalent to pa_cache_append with one new token per sequence (row b of k_new / v_new
+ * is sequence b's token, at position context_lens[b] - 1; its slot is written to
+ * slots[b] if slots is not null) followed by pa_decode on the same arguments: the same
+ * cache bytes, slots and outputs.  Inside one call the library knows that the cache write
+ * touches nothing the decode's work planning reads, so the planning runs beside the
+ * cache write instead of after it.  This is one decode step as the pages describe it:
+ * the new token's K and V join the cache kept for every token seen so far, in the block
+ * its position maps to through the table, and the token attends over the whole context
+ * ("PagedAttention and Continuous Batching Explained (2026)", sections "Why the KV cache
+ * is the problem" and "PagedAttention: a block table for the KV cache").
+ *
+ *   k_new / v_new  [num_seqs, num_kv_heads, head_dim] of dtype, 16-byte aligned
+ *   slots          int64 [num_seqs] or null
+ * Every other argument, error and status bit as in pa_decode and pa_cache_append (a
+ * context length below 1 has no position for the new token: PA_STATUS_BAD_CONTEXT).
+ */
+int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k_new,
+                     const void* v_new, void* k_cache, void* v_cache, int64_t* slots,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_decode_shared_prefix -- pa_decode for a batch in which some sequences share one
  * physical prefix.
  *

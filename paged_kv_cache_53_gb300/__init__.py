@@ -65,6 +65,8 @@ _SIGNATURES = {
                                  _p, _i, _p, _i, _f, _i, _p, _sz, _p], _i),
     "pa_decode": ([_p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz,
                    _p], _i),
+    "pa_decode_append": ([_p, _i, _p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i,
+                          _i, _f, _i, _p, _sz, _p], _i),
     "pa_prefill_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "pa_prefill_chunk": ([_p, _i, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                           _i, _f, _i, _p, _sz, _p], _i),
@@ -211,6 +213,25 @@ def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
                            _ptr(context_lens), max_ctx, b, h_q, h_kv, d, bs, nb, float(scale),
                            dtype_code(k_cache.dtype), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                  k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                  context_lens: torch.Tensor, max_ctx: int, scale: float,
+                  workspace: torch.Tensor, slots: Optional[torch.Tensor] = None, stream=None):
+    """One decode step (see pa_decode_append): row b of k_new / v_new is written at
+    position context_lens[b] - 1 of sequence b (its slot into `slots` if given), then the
+    decode attends over every context."""
+    nb, h_kv, bs, d = k_cache.shape
+    b, h_q, _ = q.shape
+    if slots is not None and slots.dtype != torch.int64:
+        raise TypeError("slots must be int64")
+    _check(lib().pa_decode_append(_ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_new),
+                                  _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slots),
+                                  _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                  max_ctx, b, h_q, h_kv, d, bs, nb, float(scale),
+                                  dtype_code(k_cache.dtype), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def decode_shared_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,

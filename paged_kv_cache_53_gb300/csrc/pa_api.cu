@@ -368,41 +368,41 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
                                 block_size);
 }
 
-int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
-              const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
-              const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
-              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-              pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  g_error[0] = '\0';
-  int rc = check_cache_geometry("pa_decode", num_kv_heads, head_dim, block_size, num_blocks,
-                                dtype);
+}  // extern "C"
+
+// Checks pa_decode's arguments (naming `who` in errors) and fills the launch arguments.
+static int decode_args(const char* who, void* out, pa_dtype out_dtype, const void* q,
+                       const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_ctx,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, pa_dtype dtype,
+                       void* workspace, size_t workspace_bytes, DecodeArgs& a) {
+  int rc = check_cache_geometry(who, num_kv_heads, head_dim, block_size, num_blocks, dtype);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || max_ctx < 0 || num_q_heads <= 0)
-    return fail(PA_ERR_INVALID_ARG, "pa_decode: negative sizes");
-  if (num_seqs == 0) return PA_OK;
+    return fail(PA_ERR_INVALID_ARG, "%s: negative sizes", who);
   if (!valid_dtype(out_dtype) || (out_dtype != dtype && out_dtype != PA_F32))
-    return fail(PA_ERR_INVALID_ARG, "pa_decode: out_dtype must equal dtype or be PA_F32");
+    return fail(PA_ERR_INVALID_ARG, "%s: out_dtype must equal dtype or be PA_F32", who);
   if (num_q_heads % num_kv_heads != 0)
-    return fail(PA_ERR_INVALID_ARG, "pa_decode: num_q_heads %d not a multiple of num_kv_heads %d",
+    return fail(PA_ERR_INVALID_ARG, "%s: num_q_heads %d not a multiple of num_kv_heads %d", who,
                 num_q_heads, num_kv_heads);
   if (!supported_group(num_q_heads / num_kv_heads))
-    return fail(PA_ERR_UNSUPPORTED, "pa_decode: group size %d not built (1, 2, 4, 8, 16)",
+    return fail(PA_ERR_UNSUPPORTED, "%s: group size %d not built (1, 2, 4, 8, 16)", who,
                 num_q_heads / num_kv_heads);
-  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq <= 0");
-  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale is NaN");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq <= 0", who);
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "%s: scale is NaN", who);
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
-    return fail(PA_ERR_INVALID_ARG, "pa_decode: null pointer");
+    return fail(PA_ERR_INVALID_ARG, "%s: null pointer", who);
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(workspace))
-    return fail(PA_ERR_INVALID_ARG, "pa_decode: out/q/caches/workspace must be 16-byte aligned");
+    return fail(PA_ERR_INVALID_ARG, "%s: out/q/caches/workspace must be 16-byte aligned", who);
   const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                              max_ctx, block_size);
   if (workspace_bytes < need)
-    return fail(PA_ERR_WORKSPACE, "pa_decode: workspace %zu bytes < %zu needed", workspace_bytes,
+    return fail(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
                 need);
   int32_t* st = status_word();
-  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_decode: no usable CUDA device");
-  DecodeArgs a;
+  if (st == nullptr) return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
   a.out = out;
   a.out_dtype = out_dtype;
   a.q = q;
@@ -424,7 +424,62 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
                                 block_size);
   a.status = st;
   a.prefix = PrefixPlan{};
+  return PA_OK;
+}
+
+extern "C" {
+
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
+              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+              pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  if (num_seqs == 0 && max_ctx >= 0 && num_q_heads > 0 &&
+      check_cache_geometry("pa_decode", num_kv_heads, head_dim, block_size, num_blocks, dtype) ==
+          PA_OK)
+    return PA_OK;
+  DecodeArgs a;
+  const int rc = decode_args("pa_decode", out, out_dtype, q, k_cache, v_cache, block_tables,
+                             max_blocks_per_seq, context_lens, max_ctx, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                             workspace, workspace_bytes, a);
+  if (rc != PA_OK) return rc;
   return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k_new,
+                     const void* v_new, void* k_cache, void* v_cache, int64_t* slots,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int max_ctx, int num_seqs, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  if (num_seqs == 0 && max_ctx >= 0 && num_q_heads > 0 &&
+      check_cache_geometry("pa_decode_append", num_kv_heads, head_dim, block_size, num_blocks,
+                           dtype) == PA_OK)
+    return PA_OK;
+  if (num_seqs > 0 && (!k_new || !v_new))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_append: null pointer");
+  if (num_seqs > 0 && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_append: K/V pointers must be 16-byte aligned");
+  DecodeArgs a;
+  int rc = decode_args("pa_decode_append", out, out_dtype, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, max_ctx, num_seqs, num_q_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                       workspace_bytes, a);
+  if (rc != PA_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the new token of sequence b is row b of k_new / v_new (no cu_q_lens: one per sequence)
+  cudaError_t e = launch_cache_append(k_new, v_new, k_cache, v_cache, slots, block_tables,
+                                      max_blocks_per_seq, nullptr, context_lens, num_seqs,
+                                      num_seqs, 1, num_kv_heads, head_dim, block_size, num_blocks,
+                                      dtype_bytes(dtype), a.status, s);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode_append: %s", cudaGetErrorString(e));
+  // the cache write neither reads nor writes what the plan uses: the plan builds the work
+  // list beside it and waits for it only before it exits
+  a.plan_wait_late = true;
+  return launch_decode(a, s);
 }
 
 // Partial slots the prefix's splits add to the decode workspace (none without sharers,

@@ -90,8 +90,9 @@ __global__ void __launch_bounds__(256) cache_append_kernel(
   griddep_launch_dependents();
   __shared__ long long s_slot[kAppendTokens];
   const int b = blockIdx.y;
-  const int first = __ldg(cu_q_lens + b);
-  const int n_new = __ldg(cu_q_lens + b + 1) - first;
+  // no cu_q_lens: one new token per sequence, token b for sequence b (a decode step)
+  const int first = cu_q_lens != nullptr ? __ldg(cu_q_lens + b) : b;
+  const int n_new = cu_q_lens != nullptr ? __ldg(cu_q_lens + b + 1) - first : 1;
   const int i0 = blockIdx.x * kAppendTokens;
   if (i0 >= n_new) return;
   const int nt = min(kAppendTokens, n_new - i0);

@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
                                                            int num_kv_heads, int block_size,
                                                            DecodeWorkspace ws, int32_t* status,
                                                            int4* out, int out_row_vec16,
-                                                           PrefixPlan pre) {
-  griddep_wait();
+                                                           PrefixPlan pre, int wait_late) {
+  // wait_late: the previous kernel on the stream writes nothing this kernel reads or
+  // writes; it is waited for only at the end, so that the work list is built meanwhile
+  // and the next kernel still starts after both (lengths are read through L2)
+  if (!wait_late) griddep_wait();
   griddep_launch_dependents();
   __shared__ long long s_sum[32];
   __shared__ int s_off[32];
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
 
   long long sum = 0;
   for (int b = b0; b < b1; ++b) {
-    const int c = context_lens[b];
+    const int c = __ldcg(context_lens + b);
     if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
     const int cc = clamp_ctx(c, ctx_cap), st = start_of(b);
     if (cc < st) flag_status(status, PA_STATUS_BAD_CONTEXT);
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
-  auto suffix_of = [&](int b) { return max(0, clamp_ctx(context_lens[b], ctx_cap) - start_of(b)); };
+  auto suffix_of = [&](int b) { return max(0, clamp_ctx(__ldcg(context_lens + b), ctx_cap) - start_of(b)); };
 
   // Counting pass.  Every lane runs `per` iterations (so that whole warps meet in the
   // shuffles and matches), and shared counters are bumped once per warp and distinct key.
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     ws.header[3] = s_total;
     ws.header[4] = s_nmerge;
   }
+  if (wait_late) griddep_wait();
 }
 
 // A unit is (partition, KV head): unit u is partition u / H_kv for KV head u % H_kv.
@@ -1026,7 +1030,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int plan_threads = std::min(1024, std::max(32, (a.num_seqs + 31) / 32 * 32));
   cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(plan_threads), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
-                             static_cast<int4*>(a.out), out_row_vec16, a.prefix);
+                             static_cast<int4*>(a.out), out_row_vec16, a.prefix,
+                             a.plan_wait_late ? 1 : 0);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
   if (a.prefix.num_sharers > 0) {
     const int rc = launch_shared_prefix(a, stream);

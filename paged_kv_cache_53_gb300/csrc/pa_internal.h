@@ -141,6 +141,10 @@ struct DecodeArgs {
   DecodeWorkspace ws;
   int32_t* status;
   PrefixPlan prefix;  // num_sharers = 0: no shared prefix
+  // The plan kernel may run beside the kernel launched just before it on the stream and
+  // wait for it only before it exits: set when that kernel is known not to write what the
+  // plan reads (context lengths, sharers) nor the output rows it zeroes.
+  bool plan_wait_late = false;
 };
 
 // Attention of a shared prefix for all of its sharers (pa_shared_prefix.cu): writes

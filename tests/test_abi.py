@@ -87,6 +87,34 @@ def test_zero_sequences_is_a_no_op(lib):
     assert _decode(lib, B=0, out=None, q=None) == 0
 
 
+def _decode_append(lib, **kw):
+    a = dict(out=FAKE, out_dtype=2, q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, slots=None,
+             bt=FAKE, maxblk=8, ctx=FAKE, max_ctx=128, B=4, Hq=32, Hkv=8, D=128, BS=16, NB=64,
+             scale=0.1, dt=2, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.pa_decode_append(a["out"], a["out_dtype"], a["q"], a["kn"], a["vn"], a["k"],
+                                a["v"], a["slots"], a["bt"], a["maxblk"], a["ctx"], a["max_ctx"],
+                                a["B"], a["Hq"], a["Hkv"], a["D"], a["BS"], a["NB"], a["scale"],
+                                a["dt"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(kn=None), 1, "null"),
+    (dict(vn=FAKE + 8), 1, "aligned"),
+    (dict(q=None), 1, "null"),
+    (dict(D=96), 2, "head_dim"),
+    (dict(ws_bytes=16), 3, "workspace"),
+    (dict(Hq=30), 1, "multiple"),
+])
+def test_decode_append_rejects_bad_arguments(lib, kw, code, needle):
+    assert _decode_append(lib, **kw) == code
+    assert "pa_decode_append" in _err(lib) and needle in _err(lib)
+
+
+def test_decode_append_zero_sequences_is_a_no_op(lib):
+    assert _decode_append(lib, B=0, out=None, q=None, kn=None, vn=None) == 0
+
+
 def test_workspace_bytes_grow_with_context(lib):
     f = lib.pa_decode_workspace_bytes
     small = f(256, 32, 8, 128, 8192, 16)
