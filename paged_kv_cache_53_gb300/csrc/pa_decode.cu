@@ -26,7 +26,7 @@
 //
 // The decode is bound by HBM: every context token's K and V row is read once and each
 // byte feeds ~1 (MHA) to ~8 (group of 8) flops, far below the ridge point.  The design
-// therefore aims at bytes in flight (up to ~190 KiB of TMA copies per SM) and keeps the
+// therefore aims at bytes in flight (up to 192 KiB of TMA copies per SM) and keeps the
 // per-tile instruction count small.
 #include <algorithm>
 #include <mutex>
@@ -455,12 +455,15 @@ MergeKernel merge_kernel_for(pa_dtype out) {
 // ----------------------------------------------------------------------------------
 template <int D, int BS, int EB>
 struct MmaCfg {
-  static constexpr int kPairs = 4;                       // producer/consumer warp pairs
+  // producer/consumer warp pairs: three consumers keep up with HBM, and the fewer the
+  // pairs the deeper each ring, which the last pairs at work in a CTA draw on at the end
+  // (three pairs of 64 KiB against four of 48 KiB: -1%; two of 96 KiB are consumer-bound)
+  static constexpr int kPairs = 3;
   static constexpr int kBoxBytes = BS * 128;             // BS rows x 64 elements (128 B)
   static constexpr int kHalves = D / 64;                 // boxes per K (or V) tile
   static constexpr int kTileBytes = kHalves * kBoxBytes;  // one K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kRingBytesPerPair = 48 * 1024;
+  static constexpr int kRingBytesPerPair = 64 * 1024;
   static constexpr int kStages =
       kRingBytesPerPair / kStageBytes > 8 ? 8 : kRingBytesPerPair / kStageBytes;
   static constexpr int kThreads = 2 * kPairs * 32;
