@@ -652,10 +652,13 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2, P>::kThreads, 1)
       const uint32_t vbase = kbase + C::kTileBytes;
 
       // scores: S[16 x BS] = Qpad[16 x D] . K^T
-      float sc[NT][4];
+      // two accumulators per 8-token tile (even and odd k-steps): dependent chains of
+      // D / 32 instead of D / 16 MMAs
+      float sc[NT][4], sd[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.f;
         const int tok = nt * 8 + (lane & 7);
 #pragma unroll
         for (int kk2 = 0; kk2 < D / 32; ++kk2) {
@@ -665,8 +668,10 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2, P>::kThreads, 1)
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
           M::run(sc[nt], qa[2 * kk2], b0, b1);
-          M::run(sc[nt], qa[2 * kk2 + 1], b2, b3);
+          M::run(sd[nt], qa[2 * kk2 + 1], b2, b3);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
       }
       // scale into log2 units; tokens past the context never count
       const int limit = d.ntok - t * BS;
