@@ -13,7 +13,9 @@
 //                reads the unit's block-table entries, and streams every (block, KV
 //                head) K and V tile into a ring of shared-memory stages with TMA; the
 //                consumer warp runs q.K^T and P.V on the tensor cores (mma.sync
-//                m16n8k16, the query group padded to 16 rows) with an online softmax.
+//                m16n8k16) with an online softmax: for groups of up to 8 rows the
+//                products are taken transposed (tokens or dimensions as M, the group's
+//                rows as N = 8), larger groups are padded to 16 rows.
 //                A unit covering a whole context writes the normalised output; the
 //                others write an fp32 partial (running max, sum, unnormalised output).
 //   3. merge  -- one warp per (sequence, query head) of a listed sequence merges its
@@ -481,6 +483,216 @@ struct MmaCfg {
   }
 };
 
+// Consumer warp for query groups of up to 8 rows.  The products are taken transposed, so
+// that a tile's 16 tokens (or 16 dimensions) are the MMA's M and the group's rows its
+// N = 8 (m16n8k16), half the MMAs of the group padded to 16 rows:
+//   S^T[tok][row]  = K[tok][:] . Q[row][:]            A = K rows, B = Q^T
+//   O^T[dim][row] += V^T[dim][tok] . P^T[tok][row]    A = V^T (transposed ldmatrix),
+//                                                      B = P^T (movmatrix of S^T's layout)
+// Lane l holds rows 2 (l % 4) and 2 (l % 4) + 1, and tokens / dimensions l / 4 and
+// l / 4 + 8 of each 16-wide tile.  Rows >= G are zero queries and are never written.
+template <typename T, int D, int BS, typename C>
+__device__ __forceinline__ void consume_t(const DecodeParams& p, UnitDesc* mydesc,
+                                          uint8_t* myq, uint32_t qstride, uint64_t* qfull,
+                                          uint64_t* qempty, uint64_t* full, uint64_t* empty,
+                                          uint8_t* mystages, uint32_t zero_addr, int lane) {
+  using M = Mma<T>;
+  constexpr int S = C::kStages;
+  constexpr int MT = BS / 16;  // 16-token tiles of S^T per K/V tile
+  constexpr int KS = D / 16;   // k-steps of K.q
+  constexpr int DT = D / 16;   // 16-dimension tiles of O^T
+  const int G = p.group;
+  const int q4 = lane & 3, g8 = lane >> 2;
+  uint32_t tile_it = 0, q_it = 0;
+  for (;;) {
+    const int qs = q_it & 1;
+    if (!mbar_wait(smem_addr(qfull + qs), (q_it >> 1) & 1)) {
+      if (lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+      return;
+    }
+    const UnitDesc d = mydesc[qs];
+    if (!d.valid) return;
+
+    // Q^T as B fragments: qb[k][0] = Q[row l/4][dims 16k + 2 (l%4), +1], qb[k][1] the same
+    // 8 dims on; one ldmatrix x4 reads two k-steps (16-byte chunks 2k .. 2k + 3)
+    uint32_t qb[KS][2];
+    {
+      const int r = lane & 7, i = lane >> 3;
+      const uint32_t rowbase = smem_addr(myq + qs * qstride) + r * (D * sizeof(T));
+#pragma unroll
+      for (int kk = 0; kk < KS; kk += 2) {
+        const uint32_t addr = r < G ? rowbase + (2 * kk + i) * 16 : zero_addr;
+        ldsm_x4(addr, qb[kk][0], qb[kk][1], qb[kk + 1][0], qb[kk + 1][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(qempty + qs));
+    ++q_it;
+
+    float o[DT][4];  // O^T: [dt][0] dim 16 dt + l/4, row 2 (l%4); [1] row + 1; [2], [3] dim + 8
+#pragma unroll
+    for (int j = 0; j < DT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float mr[2] = {kNegInf, kNegInf}, lr[2] = {0.f, 0.f};  // per row: max (log2), sum
+
+    const int ntiles = (d.ntok + BS - 1) / BS;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = tile_it % S;
+      if (!mbar_wait(smem_addr(full + s), (tile_it / S) & 1)) {
+        if (lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+        return;
+      }
+      const uint32_t kbase = smem_addr(mystages + (size_t)s * C::kStageBytes);
+      const uint32_t vbase = kbase + C::kTileBytes;
+
+      // S^T[16 MT tokens x 8 rows]; even and odd k-steps in two accumulators
+      float sc[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
+        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+        // ldmatrix x4 of K rows: (tok 0-7, chunk lo), (tok 8-15, lo), (0-7, hi), (8-15, hi)
+        const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int cg = 2 * kk + (lane >> 4);
+          const uint32_t addr =
+              kbase + (cg >> 3) * C::kBoxBytes + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
+          uint32_t a[4];
+          ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+          if (kk & 1) M::run(sd, a, qb[kk][0], qb[kk][1]);
+          else M::run(sc[mt], a, qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[mt][e] += sd[e];
+      }
+      // scale into log2 units; tokens past the context never count
+      const int limit = d.ntok - t * BS;
+      float mx[2] = {kNegInf, kNegInf};
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool valid = 16 * mt + g8 + 8 * (e >> 1) < limit;
+          sc[mt][e] = valid ? sc[mt][e] * p.scale_log2 : kNegInf;
+          mx[e & 1] = fmaxf(mx[e & 1], sc[mt][e]);
+        }
+      }
+      // a row's tokens are spread over the 8 lanes with the same l % 4
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(~0u, mx[0], off));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(~0u, mx[1], off));
+      }
+      const bool need0 = mx[0] > mr[0] + kRescaleThreshold;
+      const bool need1 = mx[1] > mr[1] + kRescaleThreshold;
+      if (__any_sync(~0u, need0 || need1)) {
+        if (need0) {
+          const float a = fast_exp2(mr[0] - mx[0]);
+          mr[0] = mx[0];
+          lr[0] *= a;
+#pragma unroll
+          for (int j = 0; j < DT; ++j) { o[j][0] *= a; o[j][2] *= a; }
+        }
+        if (need1) {
+          const float a = fast_exp2(mr[1] - mx[1]);
+          mr[1] = mx[1];
+          lr[1] *= a;
+#pragma unroll
+          for (int j = 0; j < DT; ++j) { o[j][1] *= a; o[j][3] *= a; }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sc[mt][e] = fast_exp2(sc[mt][e] - mr[e & 1]);
+          lr[e & 1] += sc[mt][e];
+        }
+      }
+      // O^T += V^T . P^T, one 16-token k-step per S^T tile, P^T carried as hi + lo terms:
+      // S^T's fragment rows are tokens, a B fragment's are rows of the group, so each
+      // 8 x 8 block of packed P^T is transposed across the warp
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t l0, l1;
+        const uint32_t h0 = movmatrix_trans(M::pack_split(sc[mt][0], sc[mt][1], l0));
+        const uint32_t h1 = movmatrix_trans(M::pack_split(sc[mt][2], sc[mt][3], l1));
+        l0 = movmatrix_trans(l0);
+        l1 = movmatrix_trans(l1);
+        // V rows of tokens past the context may hold anything (even NaN bits) and meet
+        // P = 0: clear them in the fragments of the last tile
+        const int vlim = limit - 16 * mt;
+        const bool tail = vlim < 16;
+        const uint32_t m_lo = (2 * q4 < vlim ? 0x0000ffffu : 0u) | (2 * q4 + 1 < vlim ? 0xffff0000u : 0u);
+        const uint32_t m_hi =
+            (2 * q4 + 8 < vlim ? 0x0000ffffu : 0u) | (2 * q4 + 9 < vlim ? 0xffff0000u : 0u);
+        // ldmatrix x4 .trans of V rows: (tok 0-7, chunk 2dt), (0-7, 2dt+1), (8-15, 2dt),
+        // (8-15, 2dt+1) give the A fragments of V^T for dims 16 dt .. 16 dt + 15
+        const int tok = 16 * mt + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          const int cg = 2 * dt + ((lane >> 3) & 1);
+          const uint32_t addr =
+              vbase + (cg >> 3) * C::kBoxBytes + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
+          uint32_t a[4];
+          ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+          if (tail) {
+            a[0] &= m_lo;
+            a[1] &= m_lo;
+            a[2] &= m_hi;
+            a[3] &= m_hi;
+          }
+          M::run(o[dt], a, h0, h1);
+          M::run(o[dt], a, l0, l1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(empty + s));
+      ++tile_it;
+    }
+
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lr[0] += __shfl_xor_sync(~0u, lr[0], off);
+      lr[1] += __shfl_xor_sync(~0u, lr[1], off);
+    }
+    const int hq0 = d.h * G;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int row = 2 * q4 + i;
+      if (row >= G) continue;
+      if (d.nparts == 1) {
+        const float inv = 1.f / lr[i];
+        const size_t at = ((size_t)d.b * p.num_q_heads + hq0 + row) * D + g8;
+        if (p.out_f32) {
+          float* out = static_cast<float*>(p.out) + at;
+#pragma unroll
+          for (int j = 0; j < DT; ++j) {
+            out[16 * j] = o[j][i] * inv;
+            out[16 * j + 8] = o[j][2 + i] * inv;
+          }
+        } else {
+          T* out = static_cast<T*>(p.out) + at;
+#pragma unroll
+          for (int j = 0; j < DT; ++j) {
+            store1(out + 16 * j, o[j][i] * inv);
+            store1(out + 16 * j + 8, o[j][2 + i] * inv);
+          }
+        }
+      } else {
+        const size_t slot = (size_t)d.part_idx * p.num_q_heads + hq0 + row;
+        float* acc = p.ws.part_acc + slot * D + g8;
+#pragma unroll
+        for (int j = 0; j < DT; ++j) {
+          acc[16 * j] = o[j][i];
+          acc[16 * j + 8] = o[j][2 + i];
+        }
+        if (g8 == 0) p.ws.part_ml[slot] = make_float2(mr[i], lr[i]);
+      }
+    }
+  }
+}
+
 template <typename T, int D, int BS, int P>
 __global__ void __launch_bounds__(MmaCfg<D, BS, 2, P>::kThreads, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -610,6 +822,11 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2, P>::kThreads, 1)
   const int g0 = lane >> 2, c4 = lane & 3;
   const bool hi_rows = G > 8;  // rows 8..15 of the padded query group are real
   const uint32_t zero_addr = smem_addr(zero16);
+  if (G <= 8) {
+    consume_t<T, D, BS, C>(p, mydesc, myq, qstride, qfull, qempty, full, empty, mystages,
+                           zero_addr, lane);
+    return;
+  }
   uint32_t tile_it = 0, q_it = 0;
   for (;;) {
     const int qs = q_it & 1;

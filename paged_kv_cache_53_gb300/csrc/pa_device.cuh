@@ -144,6 +144,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "r"(addr));
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit elements held one 32-bit register per lane in
+// the mma fragment layout (lane l: row l / 4, columns 2 (l % 4), +1): afterwards lane l
+// holds row l / 4 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // Packed fp32 pairs (the f32x2 arithmetic of sm_100-class SMs): one packed FMA does the
 // work of two.  In the tcgen05 kernels every instruction of the softmax warps competes
 // with the MMA-issuing thread for its scheduler's issue slots.
