@@ -455,20 +455,18 @@ MergeKernel merge_kernel_for(pa_dtype out) {
 // ----------------------------------------------------------------------------------
 // 2a. attend: TMA + tensor cores (fp16 / bf16)
 // ----------------------------------------------------------------------------------
-// P producer/consumer warp pairs per SM, each with its own ring, 192 KiB in all.  Three
-// pairs of 64 KiB suit a batch streamed from HBM: three consumers keep up with it, and the
-// last pairs at work in a CTA draw on the deeper rings at the end (~1% over four pairs on
-// the Llama- and OPT-shaped batches).  Four pairs of 48 KiB suit work the consumers'
-// arithmetic paces: many short units, or K/V that L2 holds because many sequences read
-// it (the suffixes of a shared-prefix batch: 7% over three pairs).
-template <int D, int BS, int EB, int P>
+// Four producer/consumer warp pairs per SM, each with a 48 KiB ring, 192 KiB in all.  Three
+// pairs of 64 KiB come within 0.3-0.6% on batches streamed from HBM but lose 18% where the
+// consumers' arithmetic sets the pace (K/V that L2 holds because many sequences read it);
+// two pairs of 96 KiB lose everywhere.
+template <int D, int BS, int EB>
 struct MmaCfg {
-  static constexpr int kPairs = P;
+  static constexpr int kPairs = 4;
   static constexpr int kBoxBytes = BS * 128;             // BS rows x 64 elements (128 B)
   static constexpr int kHalves = D / 64;                 // boxes per K (or V) tile
   static constexpr int kTileBytes = kHalves * kBoxBytes;  // one K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kRingBytesPerPair = P == 3 ? 64 * 1024 : 48 * 1024;
+  static constexpr int kRingBytesPerPair = 48 * 1024;
   static constexpr int kStages =
       kRingBytesPerPair / kStageBytes > 8 ? 8 : kRingBytesPerPair / kStageBytes;
   static constexpr int kThreads = 2 * kPairs * 32;
@@ -693,11 +691,11 @@ __device__ __forceinline__ void consume_t(const DecodeParams& p, UnitDesc* mydes
   }
 }
 
-template <typename T, int D, int BS, int P>
-__global__ void __launch_bounds__(MmaCfg<D, BS, 2, P>::kThreads, 1)
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-  using C = MmaCfg<D, BS, 2, P>;
+  using C = MmaCfg<D, BS, 2>;
   using M = Mma<T>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -1134,16 +1132,16 @@ int configure(KernelSlot& k, int dev, int threads, size_t smem_launch) {
   return k.occupancy[dev];
 }
 
-template <typename T, int D, int BS, int P>
+template <typename T, int D, int BS>
 KernelSlot& mma_slot() {
-  static KernelSlot slot = {reinterpret_cast<const void*>(&decode_mma_kernel<T, D, BS, P>),
-                            MmaCfg<D, BS, 2, P>::smem_bytes(kMaxGroup), {}, {}};
+  static KernelSlot slot = {reinterpret_cast<const void*>(&decode_mma_kernel<T, D, BS>),
+                            MmaCfg<D, BS, 2>::smem_bytes(kMaxGroup), {}, {}};
   return slot;
 }
 
-template <typename T, int D, int BS, int P>
+template <typename T, int D, int BS>
 int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
-  using C = MmaCfg<D, BS, 2, P>;
+  using C = MmaCfg<D, BS, 2>;
   CUtensorMap tmk, tmv;
   int r1 = encode_cache_map(&tmk, a.k_cache, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
                             a.head_dim);
@@ -1153,32 +1151,24 @@ int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) 
     return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed (%d, %d)", r1, r2);
   int dev = 0;
   cudaGetDevice(&dev);
-  KernelSlot& slot = mma_slot<T, D, BS, P>();
+  KernelSlot& slot = mma_slot<T, D, BS>();
   const int occ = configure(slot, dev, C::kThreads, slot.smem_max);
   if (occ < 0) return fail(PA_ERR_CUDA, "pa_decode: kernel configuration failed");
   const int grid = sm_count() * occ;
-  const cudaError_t e = launch_pdl(decode_mma_kernel<T, D, BS, P>, dim3(grid), dim3(C::kThreads),
+  const cudaError_t e = launch_pdl(decode_mma_kernel<T, D, BS>, dim3(grid), dim3(C::kThreads),
                                    C::smem_bytes(p.group), stream, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
   return PA_OK;
 }
 
-template <typename T, int P>
-int launch_mma_pairs(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
-  if (a.head_dim == 128 && a.block_size == 16) return launch_mma<T, 128, 16, P>(a, p, stream);
-  if (a.head_dim == 128 && a.block_size == 32) return launch_mma<T, 128, 32, P>(a, p, stream);
-  if (a.head_dim == 64 && a.block_size == 16) return launch_mma<T, 64, 16, P>(a, p, stream);
-  if (a.head_dim == 64 && a.block_size == 32) return launch_mma<T, 64, 32, P>(a, p, stream);
-  return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim %d / block_size %d", a.head_dim,
-              a.block_size);
-}
-
-// With a shared prefix the attention kernel sees only the sequences' own short suffixes
-// (the prefix goes through its own kernel): four pairs; otherwise three.
 template <typename T>
 int launch_mma_dispatch(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
-  return a.prefix.num_sharers > 0 ? launch_mma_pairs<T, 4>(a, p, stream)
-                                  : launch_mma_pairs<T, 3>(a, p, stream);
+  if (a.head_dim == 128 && a.block_size == 16) return launch_mma<T, 128, 16>(a, p, stream);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_mma<T, 128, 32>(a, p, stream);
+  if (a.head_dim == 64 && a.block_size == 16) return launch_mma<T, 64, 16>(a, p, stream);
+  if (a.head_dim == 64 && a.block_size == 32) return launch_mma<T, 64, 32>(a, p, stream);
+  return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim %d / block_size %d", a.head_dim,
+              a.block_size);
 }
 
 }  // namespace
