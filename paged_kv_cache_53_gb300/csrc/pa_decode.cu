@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   __shared__ int s_off[32];
   __shared__ int s_hist[kMaxPartBlocks + 2];
   __shared__ int s_psz, s_total, s_units, s_nmerge;
+  // each sequence's own context (past a shared prefix), read once from memory: the later
+  // passes take it from here (each thread reads back only what it wrote)
+  constexpr int kSufCache = 4096;
+  __shared__ int s_suf[kSufCache];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
   const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     const int cc = clamp_ctx(c, ctx_cap), st = start_of(b);
     if (cc < st) flag_status(status, PA_STATUS_BAD_CONTEXT);
     sum += max(0, cc - st);
+    if (b < kSufCache) s_suf[b] = max(0, cc - st);
     if (cc == 0 && reserved_of(b) == 0)  // an empty context attends to nothing: zeros
       for (int i = 0; i < out_row_vec16; ++i) out[(size_t)b * out_row_vec16 + i] = make_int4(0, 0, 0, 0);
   }
@@ -152,7 +157,10 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
-  auto suffix_of = [&](int b) { return max(0, clamp_ctx(__ldcg(context_lens + b), ctx_cap) - start_of(b)); };
+  auto suffix_of = [&](int b) {
+    return b < kSufCache ? s_suf[b]
+                         : max(0, clamp_ctx(__ldcg(context_lens + b), ctx_cap) - start_of(b));
+  };
 
   // Counting pass.  Every lane runs `per` iterations (so that whole warps meet in the
   // shuffles and matches), and shared counters are bumped once per warp and distinct key.
