@@ -249,6 +249,8 @@ def run_ours(args, rank, world, local_rank):
     share = d is not None and step.shared_prefix is not None and args.share_prefix == "on"
     # a plain decode batch takes the fused step call (cache write + decode)
     fused_decode = d is not None and not share and args.decode_append == "on"
+    # a batch with both kinds takes the mixed-step call (decode and prefill side by side)
+    mixed = fused_decode and p is not None and args.mixed_step == "on"
     if d is not None:
         out_dec = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=tdt, device=dev)
         if share:
@@ -287,6 +289,21 @@ def run_ours(args, rank, world, local_rank):
         if pairs is not None:
             pa.copy_blocks([kc], [vc], pairs)
             n += 1
+        if mixed and ev is None:
+            # decode and prefill side by side in one call (the per-call pass runs them as
+            # separate calls, so that each has a duration of its own)
+            md, mp = io["decode"], io["prefill"]
+            pa.mixed_step(
+                kc, vc, step.scale,
+                decode=dict(out=io["out"]["decode"], q=md["q"], k_new=md["kn"], v_new=md["vn"],
+                            block_tables=md["bt"], context_lens=md["ctx"], max_ctx=d.max_ctx,
+                            workspace=ws_dec, slots=meta["decode"]["slots"]),
+                prefill=dict(out=io["out"]["prefill"], q=mp["q"], k_new=mp["kn"], v_new=mp["vn"],
+                             block_tables=mp["bt"], cu_q_lens=mp["cu"], context_lens=mp["ctx"],
+                             max_q=p.max_q, max_ctx=p.max_ctx, workspace=ws_pre,
+                             slots=meta["prefill"]["slots"]))  # the current stream (captured)
+            launches_per_step = n + 7  # decode: cache write, plan, attend, merge; prefill: 3
+            return
         for kind in meta:  # slot mapping + cache write, fused
             if kind == "decode" and fused_decode:
                 continue  # written by pa_decode_append below
@@ -322,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
                              p.max_q, p.max_ctx, step.scale, ws_pre)
             if ev is not None:
                 ev[3].record(stream)
-            n += 1
+            n += 2  # plan, attention
         launches_per_step = n
 
     def barrier():
@@ -353,6 +370,7 @@ def run_ours(args, rank, world, local_rank):
         for i in range(k):
             one_step()
         t1.record(stream)
+        step_launches = launches_per_step
         barrier()
         t2.record(stream)
         for i in range(k):
@@ -480,7 +498,9 @@ def run_ours(args, rank, world, local_rank):
         "parallelism": f"replicas x{world}",
         "timing": ("step: k steps with no event between kernels; per-call durations: a "
                    f"second pass of k steps with events around each call ({evented_ms:.5f} "
-                   "ms per step in that pass)"),
+                   "ms per step in that pass)"
+                   + ("; the step is one pa_mixed_step call (decode and prefill side by side), "
+                      "the per-call pass runs them as separate calls" if mixed else "")),
     }
     if share:
         config["shared_prefix"] = {"sharers": int(len(sharers)), "prefix_len": int(plen),
@@ -566,7 +586,7 @@ def run_ours(args, rank, world, local_rank):
                              traffic=recorded_traffic(args.workload)),
         })
     res["clocks"] = clocks.summary()
-    res["gpu_launches"] = launches_per_step * k
+    res["gpu_launches"] = step_launches * k
     return res, step
 
 
@@ -884,6 +904,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.NAMED), default="llama8b_gqa_decode")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--mixed-step", choices=["on", "off"], default="on",
+                    help="on: a batch of decodes and prefill chunks in one pa_mixed_step call "
+                         "(the two side by side on disjoint SMs); off: the calls in turn")
     ap.add_argument("--decode-append", choices=["on", "off"], default="on",
                     help="on: a plain decode batch's cache write and decode in one call "
                          "(pa_decode_append); off: pa_cache_append then pa_decode")

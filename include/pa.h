@@ -347,6 +347,67 @@ int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k
                      int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pa_mixed_step -- one serving step of a batch that mixes decodes and prefill chunks.
+ *
+ * Prefill and decode share one batch ("KV Cache in Serving Engines", section "New
+ * Problem: Long Prefills Pause Decoding"; "Continuous batching, paged attention, prefix
+ * caching", section "Throughput against latency"): here the decode half streams K/V from
+ * HBM while the prefill half keeps the tensor cores busy, so the two run side by side on
+ * disjoint SMs instead of one after the other.  The result is that of
+ *     pa_decode_append(decode batch), then
+ *     pa_cache_append(prefill batch's new tokens) + pa_prefill_chunk(prefill batch):
+ * the same cache bytes, slots and outputs.  The decode runs on `stream`, its attention
+ * kernel on about 58% of the SMs; the prefill runs on a stream of the library's own that
+ * waits for the work enqueued on `stream` before the call, and `stream` waits for it
+ * before any later work (so the call is stream-ordered as usual, under graph capture
+ * too).  The two batches must not share sequences.
+ *
+ *   dec   the decode batch: one new token per sequence (row b of k_new / v_new), as in
+ *         pa_decode_append; null or num_seqs = 0 for none
+ *   pre   the prefill batch: num_tokens new tokens in chunks cu_q_lens, as in
+ *         pa_cache_append + pa_prefill_chunk; null or num_seqs = 0 for none
+ * Errors and status bits as in those calls (the message names pa_mixed_step).
+ */
+typedef struct {
+  void* out;                   /* [num_seqs, num_q_heads, head_dim] of out_dtype */
+  pa_dtype out_dtype;          /* dtype or PA_F32 */
+  const void* q;               /* [num_seqs, num_q_heads, head_dim] of dtype */
+  const void* k_new;           /* [num_seqs, num_kv_heads, head_dim] of dtype */
+  const void* v_new;
+  int64_t* slots;              /* int64 [num_seqs] or null */
+  const int32_t* block_tables; /* int32 [num_seqs, max_blocks_per_seq] */
+  int max_blocks_per_seq;
+  const int32_t* context_lens; /* int32 [num_seqs], the new token included */
+  int max_ctx;
+  int num_seqs;
+  void* workspace;             /* pa_decode_workspace_bytes(...) bytes */
+  size_t workspace_bytes;
+} pa_decode_batch;
+
+typedef struct {
+  void* out;                   /* [num_tokens, num_q_heads, head_dim] of out_dtype */
+  pa_dtype out_dtype;
+  const void* q;               /* [num_tokens, num_q_heads, head_dim] of dtype */
+  const void* k_new;           /* [num_tokens, num_kv_heads, head_dim] of dtype */
+  const void* v_new;
+  int64_t* slots;              /* int64 [num_tokens] or null */
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* cu_q_lens;    /* int32 [num_seqs + 1] */
+  const int32_t* context_lens; /* int32 [num_seqs], the chunk included */
+  int max_q;
+  int max_ctx;
+  int num_seqs;
+  int num_tokens;
+  void* workspace;             /* pa_prefill_workspace_bytes(...) bytes */
+  size_t workspace_bytes;
+} pa_prefill_batch;
+
+int pa_mixed_step(const pa_decode_batch* dec, const pa_prefill_batch* pre, void* k_cache,
+                  void* v_cache, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, pa_dtype dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

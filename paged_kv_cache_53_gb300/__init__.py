@@ -53,6 +53,7 @@ _SIGNATURES = {
     "pa_last_error_string": ([], ctypes.c_char_p),
     "pa_get_status": ([_p], _i),
     "pa_selftest_wait_timeout": ([_i, _p], _i),
+    "pa_mixed_step": ([_p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _i, _p], _i),
     "pa_slot_mapping": ([_p, _p, _i, _p, _p, _i, _i, _i, _i, _p], _i),
     "pa_reshape_and_cache": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _p], _i),
@@ -232,6 +233,64 @@ def decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new
                                   max_ctx, b, h_q, h_kv, d, bs, nb, float(scale),
                                   dtype_code(k_cache.dtype), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+class _DecodeBatch(ctypes.Structure):
+    """pa_decode_batch of include/pa.h."""
+    _fields_ = [("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int), ("q", ctypes.c_void_p),
+                ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("slots", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int), ("context_lens", ctypes.c_void_p),
+                ("max_ctx", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class _PrefillBatch(ctypes.Structure):
+    """pa_prefill_batch of include/pa.h."""
+    _fields_ = [("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int), ("q", ctypes.c_void_p),
+                ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("slots", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int), ("cu_q_lens", ctypes.c_void_p),
+                ("context_lens", ctypes.c_void_p), ("max_q", ctypes.c_int),
+                ("max_ctx", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("num_tokens", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+def mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
+               decode: Optional[dict] = None, prefill: Optional[dict] = None, stream=None):
+    """One step of a batch of decodes and prefill chunks run side by side (see
+    pa_mixed_step).  `decode`: out, q, k_new, v_new, block_tables, context_lens, max_ctx,
+    workspace[, slots]; `prefill`: the same plus cu_q_lens and max_q (k_new / v_new hold the
+    chunks' new tokens)."""
+    nb, h_kv, bs, d = k_cache.shape
+    h_q = None
+    dp = pp = None
+    if decode is not None:
+        m = decode
+        h_q = m["q"].shape[1]
+        ws = m["workspace"]
+        dp = _DecodeBatch(_ptr(m["out"]), dtype_code(m["out"].dtype), _ptr(m["q"]),
+                          _ptr(m["k_new"]), _ptr(m["v_new"]), _ptr(m.get("slots")),
+                          _ptr(m["block_tables"]), m["block_tables"].shape[1],
+                          _ptr(m["context_lens"]), int(m["max_ctx"]), m["q"].shape[0],
+                          _ptr(ws), ws.numel() * ws.element_size())
+    if prefill is not None:
+        m = prefill
+        h_q = m["q"].shape[1]
+        ws = m["workspace"]
+        pp = _PrefillBatch(_ptr(m["out"]), dtype_code(m["out"].dtype), _ptr(m["q"]),
+                           _ptr(m["k_new"]), _ptr(m["v_new"]), _ptr(m.get("slots")),
+                           _ptr(m["block_tables"]), m["block_tables"].shape[1],
+                           _ptr(m["cu_q_lens"]), _ptr(m["context_lens"]), int(m["max_q"]),
+                           int(m["max_ctx"]), m["cu_q_lens"].shape[0] - 1, m["q"].shape[0],
+                           _ptr(ws), ws.numel() * ws.element_size())
+    if h_q is None:
+        return
+    _check(lib().pa_mixed_step(ctypes.byref(dp) if dp is not None else None,
+                               ctypes.byref(pp) if pp is not None else None, _ptr(k_cache),
+                               _ptr(v_cache), h_q, h_kv, d, bs, nb, float(scale),
+                               dtype_code(k_cache.dtype), _stream(stream)))
 
 
 def decode_shared_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,

@@ -2,6 +2,7 @@
 // TMA descriptor encoding, and dispatch to the kernels' launchers.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -427,6 +428,20 @@ static int decode_args(const char* who, void* out, pa_dtype out_dtype, const voi
   return PA_OK;
 }
 
+// The cache write of one new token per sequence (row b of k_new / v_new for sequence b),
+// then the decode.  The cache write neither reads nor writes what the decode's plan uses:
+// the plan builds the work list beside it and waits for it only before it exits.
+static int launch_decode_append(const char* who, DecodeArgs& a, const void* k_new,
+                                const void* v_new, int64_t* slots, cudaStream_t s) {
+  const cudaError_t e = launch_cache_append(
+      k_new, v_new, const_cast<void*>(a.k_cache), const_cast<void*>(a.v_cache), slots,
+      a.block_tables, a.max_blocks, nullptr, a.context_lens, a.num_seqs, a.num_seqs, 1,
+      a.num_kv_heads, a.head_dim, a.block_size, a.num_blocks, dtype_bytes(a.dtype), a.status, s);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  a.plan_wait_late = true;
+  return launch_decode(a, s);
+}
+
 extern "C" {
 
 int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
@@ -469,17 +484,8 @@ int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k
                        num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
                        workspace_bytes, a);
   if (rc != PA_OK) return rc;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the new token of sequence b is row b of k_new / v_new (no cu_q_lens: one per sequence)
-  cudaError_t e = launch_cache_append(k_new, v_new, k_cache, v_cache, slots, block_tables,
-                                      max_blocks_per_seq, nullptr, context_lens, num_seqs,
-                                      num_seqs, 1, num_kv_heads, head_dim, block_size, num_blocks,
-                                      dtype_bytes(dtype), a.status, s);
-  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode_append: %s", cudaGetErrorString(e));
-  // the cache write neither reads nor writes what the plan uses: the plan builds the work
-  // list beside it and waits for it only before it exits
-  a.plan_wait_late = true;
-  return launch_decode(a, s);
+  return launch_decode_append("pa_decode_append", a, k_new, v_new, slots,
+                              static_cast<cudaStream_t>(stream));
 }
 
 // Partial slots the prefix's splits add to the decode workspace (none without sharers,
@@ -581,47 +587,51 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int n
                                  max_ctx, block_size);
 }
 
-int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
-                     const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
-                     const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
-                     int num_tokens, int max_q, int max_ctx, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
-                     void* workspace, size_t workspace_bytes, void* stream) {
-  g_error[0] = '\0';
-  int rc = check_cache_geometry("pa_prefill_chunk", num_kv_heads, head_dim, block_size,
-                                num_blocks, dtype);
+}  // extern "C"
+
+// Checks pa_prefill_chunk's arguments (naming `who` in errors) and fills the launch
+// arguments.  *empty is set when there is nothing to do (no sequences or tokens).
+static int prefill_args(const char* who, void* out, pa_dtype out_dtype, const void* q,
+                        const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* cu_q_lens,
+                        const int32_t* context_lens, int num_seqs, int num_tokens, int max_q,
+                        int max_ctx, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int num_blocks, float scale, pa_dtype dtype,
+                        void* workspace, size_t workspace_bytes, PrefillArgs& a, bool* empty) {
+  *empty = false;
+  int rc = check_cache_geometry(who, num_kv_heads, head_dim, block_size, num_blocks, dtype);
   if (rc != PA_OK) return rc;
   if (dtype == PA_F32)
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: fp32 runs on decode only (f16/bf16 here)");
+    return fail(PA_ERR_UNSUPPORTED, "%s: fp32 runs on decode only (f16/bf16 here)", who);
   if (num_seqs < 0 || num_tokens < 0 || max_q < 0 || max_ctx < 0 || num_q_heads <= 0)
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: negative sizes");
-  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+    return fail(PA_ERR_INVALID_ARG, "%s: negative sizes", who);
+  if (num_seqs == 0 || num_tokens == 0) {
+    *empty = true;
+    return PA_OK;
+  }
   if (!valid_dtype(out_dtype) || (out_dtype != dtype && out_dtype != PA_F32))
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: out_dtype must equal dtype or be PA_F32");
+    return fail(PA_ERR_INVALID_ARG, "%s: out_dtype must equal dtype or be PA_F32", who);
   if (num_q_heads % num_kv_heads != 0)
-    return fail(PA_ERR_INVALID_ARG,
-                "pa_prefill_chunk: num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
-                num_kv_heads);
+    return fail(PA_ERR_INVALID_ARG, "%s: num_q_heads %d not a multiple of num_kv_heads %d", who,
+                num_q_heads, num_kv_heads);
   if (!supported_group(num_q_heads / num_kv_heads))
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: group size %d not built",
-                num_q_heads / num_kv_heads);
+    return fail(PA_ERR_UNSUPPORTED, "%s: group size %d not built", who, num_q_heads / num_kv_heads);
   if (max_blocks_per_seq <= 0 || max_q <= 0)
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: max_blocks_per_seq and max_q must be > 0");
-  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: scale is NaN");
+    return fail(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq and max_q must be > 0", who);
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "%s: scale is NaN", who);
   if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_q_lens || !context_lens)
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: null pointer");
+    return fail(PA_ERR_INVALID_ARG, "%s: null pointer", who);
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: out/q/caches must be 16-byte aligned");
+    return fail(PA_ERR_INVALID_ARG, "%s: out/q/caches must be 16-byte aligned", who);
   const size_t need = prefill_workspace_bytes(num_seqs, num_tokens, max_q, num_q_heads,
                                               num_kv_heads, head_dim, max_ctx, block_size);
   if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
-    return fail(PA_ERR_INVALID_ARG, "pa_prefill_chunk: workspace null or unaligned");
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace null or unaligned", who);
   if (workspace_bytes < need)
-    return fail(PA_ERR_WORKSPACE, "pa_prefill_chunk: workspace %zu bytes < %zu needed",
-                workspace_bytes, need);
+    return fail(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                need);
   int32_t* st = status_word();
-  if (st == nullptr) return fail(PA_ERR_CUDA, "pa_prefill_chunk: no usable CUDA device");
-  PrefillArgs a;
+  if (st == nullptr) return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
   a.out = out;
   a.out_dtype = out_dtype;
   a.q = q;
@@ -645,7 +655,126 @@ int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.status = st;
+  return PA_OK;
+}
+
+// Share of the SMs the decode's attention kernel takes in a mixed step: it stays bound by
+// HBM on ~58% of them (2.74 against 2.70 ms on the mixed workload's decode batch), and the
+// prefill's tensor-core work fills the rest (the step 2.85 ms against 3.13 ms in turn).
+constexpr int kMixedDecodePercent = 58;
+
+// A stream of the library's own per device and host thread, for work that runs beside the
+// caller's stream, with the two events that fork it from and join it to that stream.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static int side_stream(const char* who, SideStream** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
+  static thread_local SideStream per_dev[64];
+  SideStream& x = per_dev[dev];
+  if (x.stream == nullptr) {
+    if (cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
+      return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(cudaGetLastError()));
+  }
+  *out = &x;
+  return PA_OK;
+}
+
+// A prefill batch's cache write (its chunks' new tokens), then its attention.
+static int launch_prefill_append(const char* who, const PrefillArgs& a, const void* k_new,
+                                 const void* v_new, int64_t* slots, cudaStream_t s) {
+  const cudaError_t e = launch_cache_append(
+      k_new, v_new, const_cast<void*>(a.k_cache), const_cast<void*>(a.v_cache), slots,
+      a.block_tables, a.max_blocks, a.cu_q_lens, a.context_lens, a.num_seqs, a.num_tokens,
+      a.max_q, a.num_kv_heads, a.head_dim, a.block_size, a.num_blocks, dtype_bytes(a.dtype),
+      a.status, s);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  return launch_prefill(a, s);
+}
+
+extern "C" {
+
+int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* cu_q_lens, const int32_t* context_lens, int num_seqs,
+                     int num_tokens, int max_q, int max_ctx, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  PrefillArgs a;
+  bool empty = false;
+  const int rc = prefill_args("pa_prefill_chunk", out, out_dtype, q, k_cache, v_cache,
+                              block_tables, max_blocks_per_seq, cu_q_lens, context_lens, num_seqs,
+                              num_tokens, max_q, max_ctx, num_q_heads, num_kv_heads, head_dim,
+                              block_size, num_blocks, scale, dtype, workspace, workspace_bytes, a,
+                              &empty);
+  if (rc != PA_OK || empty) return rc;
   return launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
+int pa_mixed_step(const pa_decode_batch* dec, const pa_prefill_batch* pre, void* k_cache,
+                  void* v_cache, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, pa_dtype dtype, void* stream) {
+  g_error[0] = '\0';
+  const char* who = "pa_mixed_step";
+  const bool has_dec = dec != nullptr && dec->num_seqs != 0;
+  const bool has_pre = pre != nullptr && (pre->num_seqs != 0 || pre->num_tokens != 0);
+  if (has_dec && dec->num_seqs > 0 && (!dec->k_new || !dec->v_new))
+    return fail(PA_ERR_INVALID_ARG, "%s: decode batch: null pointer", who);
+  if (has_dec && dec->num_seqs > 0 && (!aligned16(dec->k_new) || !aligned16(dec->v_new)))
+    return fail(PA_ERR_INVALID_ARG, "%s: decode batch: K/V pointers must be 16-byte aligned", who);
+  if (has_pre && pre->num_tokens > 0 && (!pre->k_new || !pre->v_new))
+    return fail(PA_ERR_INVALID_ARG, "%s: prefill batch: null pointer", who);
+  if (has_pre && pre->num_tokens > 0 && (!aligned16(pre->k_new) || !aligned16(pre->v_new)))
+    return fail(PA_ERR_INVALID_ARG, "%s: prefill batch: K/V pointers must be 16-byte aligned", who);
+  DecodeArgs da;
+  if (has_dec) {
+    const int rc = decode_args(who, dec->out, dec->out_dtype, dec->q, k_cache, v_cache,
+                               dec->block_tables, dec->max_blocks_per_seq, dec->context_lens,
+                               dec->max_ctx, dec->num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, num_blocks, scale, dtype, dec->workspace,
+                               dec->workspace_bytes, da);
+    if (rc != PA_OK) return rc;
+  }
+  PrefillArgs pa_args;
+  bool pre_empty = true;
+  if (has_pre) {
+    const int rc = prefill_args(who, pre->out, pre->out_dtype, pre->q, k_cache, v_cache,
+                                pre->block_tables, pre->max_blocks_per_seq, pre->cu_q_lens,
+                                pre->context_lens, pre->num_seqs, pre->num_tokens, pre->max_q,
+                                pre->max_ctx, num_q_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, dtype, pre->workspace, pre->workspace_bytes,
+                                pa_args, &pre_empty);
+    if (rc != PA_OK) return rc;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!has_dec && pre_empty) return PA_OK;
+  if (!has_dec) return launch_prefill_append(who, pa_args, pre->k_new, pre->v_new, pre->slots, s);
+  if (pre_empty) return launch_decode_append(who, da, dec->k_new, dec->v_new, dec->slots, s);
+  // both: the decode on the caller's stream, launched first so that its attention kernel
+  // holds its share of the SMs before the prefill's CTAs take the rest
+  SideStream* side = nullptr;
+  int rc = side_stream(who, &side);
+  if (rc != PA_OK) return rc;
+  if (cudaEventRecord(side->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+    return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(cudaGetLastError()));
+  da.max_ctas = std::max(1, sm_count() * kMixedDecodePercent / 100);
+  rc = launch_decode_append(who, da, dec->k_new, dec->v_new, dec->slots, s);
+  // the side stream is joined back even when a launch failed, so that `stream` never
+  // runs ahead of work already enqueued beside it
+  const int rc2 = launch_prefill_append(who, pa_args, pre->k_new, pre->v_new, pre->slots,
+                                        side->stream);
+  if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+      cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+    return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(cudaGetLastError()));
+  return rc != PA_OK ? rc : rc2;
 }
 
 }  // extern "C"

@@ -1162,7 +1162,7 @@ int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) 
   KernelSlot& slot = mma_slot<T, D, BS>();
   const int occ = configure(slot, dev, C::kThreads, slot.smem_max);
   if (occ < 0) return fail(PA_ERR_CUDA, "pa_decode: kernel configuration failed");
-  const int grid = sm_count() * occ;
+  const int grid = a.max_ctas > 0 ? std::min(a.max_ctas, sm_count() * occ) : sm_count() * occ;
   const cudaError_t e = launch_pdl(decode_mma_kernel<T, D, BS>, dim3(grid), dim3(C::kThreads),
                                    C::smem_bytes(p.group), stream, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
@@ -1292,7 +1292,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {
-    const dim3 grid(std::max(1, sm_count()) * 8);
+    const int ctas = std::max(1, sm_count()) * 8;
+    const dim3 grid(a.max_ctas > 0 ? std::min(ctas, a.max_ctas * 8) : ctas);
     const float* kc = static_cast<const float*>(a.k_cache);
     const float* vc = static_cast<const float*>(a.v_cache);
     e = a.head_dim == 128

@@ -145,6 +145,9 @@ struct DecodeArgs {
   // wait for it only before it exits: set when that kernel is known not to write what the
   // plan reads (context lengths, sharers) nor the output rows it zeroes.
   bool plan_wait_late = false;
+  // at most this many CTAs for the attention kernel (0: one per SM), leaving the other SMs
+  // to work running beside it on another stream
+  int max_ctas = 0;
 };
 
 // Attention of a shared prefix for all of its sharers (pa_shared_prefix.cu): writes

@@ -188,3 +188,38 @@ def test_shared_prefix_workspace_bytes(lib):
     # every sharer keeps one fp32 partial row per query head and prefix split
     assert with_prefix >= plain + 128 * 32 * 128 * 4
     assert f(160, 30, 8, 128, 2560, 16, 128, 2048) == 0
+
+
+def _mixed_batches():
+    import paged_kv_cache_53_gb300 as pa
+    dec = pa._DecodeBatch(FAKE, 2, FAKE, FAKE, FAKE, None, FAKE, 8, FAKE, 128, 4, FAKE, 1 << 30)
+    pre = pa._PrefillBatch(FAKE, 2, FAKE, FAKE, FAKE, None, FAKE, 8, FAKE, FAKE, 64, 512, 2, 100,
+                           FAKE, 1 << 30)
+    return dec, pre
+
+
+def _mixed(lib, dec, pre):
+    return lib.pa_mixed_step(ctypes.byref(dec) if dec is not None else None,
+                             ctypes.byref(pre) if pre is not None else None, FAKE, FAKE, 32, 8,
+                             128, 16, 64, 0.1, 2, None)
+
+
+def test_mixed_step_with_nothing_to_do(lib):
+    dec, pre = _mixed_batches()
+    dec.num_seqs = 0
+    pre.num_seqs = pre.num_tokens = 0
+    assert _mixed(lib, None, None) == 0
+    assert _mixed(lib, dec, pre) == 0
+
+
+@pytest.mark.parametrize("which,field,value,needle", [
+    ("dec", "k_new", None, "decode batch: null"),
+    ("dec", "v_new", FAKE + 4, "decode batch: K/V pointers"),
+    ("pre", "k_new", None, "prefill batch: null"),
+    ("pre", "v_new", FAKE + 2, "prefill batch: K/V pointers"),
+])
+def test_mixed_step_rejects_bad_batches(lib, which, field, value, needle):
+    dec, pre = _mixed_batches()
+    setattr(dec if which == "dec" else pre, field, value)
+    assert _mixed(lib, dec, pre) == 1
+    assert "pa_mixed_step" in _err(lib) and needle in _err(lib)
