@@ -264,8 +264,9 @@ int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k
  *   prefix_len     tokens of the prefix, a multiple of block_size
  *   sharers        int32 [num_sharers], distinct indices of the sequences (rows of
  *                  block_tables) whose first prefix_len tokens are that prefix; each must
- *                  have context_lens >= prefix_len and its table must start with
- *                  prefix_blocks (not checked)
+ *                  have context_lens >= prefix_len (else PA_STATUS_BAD_CONTEXT) and its
+ *                  table must start with prefix_blocks (not checked); an index outside
+ *                  [0, num_seqs) sets PA_STATUS_BAD_CONTEXT and is skipped
  *   workspace      at least pa_decode_shared_prefix_workspace_bytes(...) bytes
  * Other arguments as in pa_decode; dtype PA_F16 or PA_BF16.  num_sharers = 0 (or
  * prefix_len = 0) is a plain decode.

@@ -48,8 +48,9 @@ struct SpCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kBars = 2 * kStages + 3 * kTiles + 1;
   static constexpr int kGatherThreads = kThreads - 32;  // every warp but the producer
+  static constexpr int kMaxSharers = kTiles * BM;  // sequences whose rows one CTA takes
   static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
-                                  kBars * 8 + 16;
+                                  kBars * 8 + 16 + kMaxSharers * 4;
 };
 
 template <typename T>
@@ -72,7 +73,7 @@ struct SpParams {
   float* part_acc;
   int32_t* status;
   int num_sharers, prefix_len, split_tokens;
-  int num_q_heads, num_kv_heads, group, num_blocks;
+  int num_seqs, num_q_heads, num_kv_heads, group, num_blocks;
   float scale_log2;
 };
 
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sKV = sQ + NT * C::kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
+  int* s_seq = reinterpret_cast<int*>(tmem_slot + 4);  // [kMaxSharers]
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + S;
   uint64_t* s_full = bars + 2 * S;
@@ -106,6 +108,14 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = (kv_end - kv_begin + BN - 1) / BN;
   const int nblk = p.prefix_len / BS;
 
+  // the sequences of this CTA's sharers (G query rows each), read while the barriers and the
+  // tensor memory are set up: -1 for an index out of range (the decode plan flags it)
+  const int si_lo = row0 / G;
+  const int si_hi = min(p.num_sharers, (row0 + NT * C::BM + G - 1) / G);
+  for (int i = threadIdx.x; si_lo + i < si_hi; i += C::kThreads) {
+    const int sb = __ldg(p.sharers + si_lo + i);
+    s_seq[i] = sb >= 0 && sb < p.num_seqs ? sb : -1;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_addr(kv_full + i), 1);
@@ -143,8 +153,9 @@ __global__ void __launch_bounds__(384, 1)
   if (warp > 0) {
     // the query rows of both tiles, gathered from their sequences into the 128-byte
     // swizzled layout while the producer's first K/V tiles are in flight (rows past the
-    // sharers read zeros); kUnroll loads in flight per thread
-    constexpr int kItems = NT * C::BM * (D / 8), kUnroll = 6;
+    // sharers read zeros); every load of a thread in flight at once
+    constexpr int kItems = NT * C::BM * (D / 8);
+    constexpr int kUnroll = (kItems + C::kGatherThreads - 1) / C::kGatherThreads;
     const int t = threadIdx.x - 32;
     for (int i0 = t; i0 < kItems; i0 += kUnroll * C::kGatherThreads) {
       uint4 v[kUnroll];
@@ -161,10 +172,12 @@ __global__ void __launch_bounds__(384, 1)
                               : ~0u;
         if (idx < kItems && grow < rows_total) {
           const int si = grow / G, g = grow - si * G;
-          const int sb = __ldg(p.sharers + si);
-          v[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                      ((size_t)sb * p.num_q_heads + h * G + g) * D) +
-                       c);
+          const int sb = s_seq[si - si_lo];
+          if (sb >= 0)
+            v[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                        ((size_t)sb * p.num_q_heads + h * G + g) *
+                                                            D) +
+                         c);
         }
       }
 #pragma unroll
@@ -385,11 +398,10 @@ __global__ void __launch_bounds__(384, 1)
     if (__all_sync(~0u, go)) {  // warp-collective loads and shuffles below
       tc::fence_after_sync();
       const int grow = row0 + x * C::BM + r;
-      const bool row_ok = grow < rows_total;
+      const int si = grow / G, g = grow - si * G;
+      const int sb = grow < rows_total ? s_seq[si - si_lo] : -1;
       float* dst = nullptr;
-      if (row_ok) {
-        const int si = grow / G, g = grow - si * G;
-        const int sb = __ldg(p.sharers + si);
+      if (sb >= 0) {
         const size_t row = (size_t)(p.part_start[sb] + split) * p.num_q_heads + h * G + g;
         p.part_ml[row] = make_float2(m, l);
         dst = p.part_acc + row * D;
@@ -467,6 +479,7 @@ int launch_t(const DecodeArgs& a, cudaStream_t stream) {
   p.num_sharers = a.prefix.num_sharers;
   p.prefix_len = a.prefix.prefix_len;
   p.split_tokens = a.prefix.split_tokens;
+  p.num_seqs = a.num_seqs;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;

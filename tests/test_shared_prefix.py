@@ -153,6 +153,23 @@ def test_sharer_shorter_than_the_prefix_is_flagged(pa):
     assert pa.get_status() & pa.STATUS_BAD_CONTEXT
 
 
+def test_sharer_index_out_of_range_is_flagged(pa):
+    """A sharer index outside the batch (past its end, or negative) sets the bad-context bit
+    and is skipped: no read of a query row or write of a partial outside the buffers, and
+    the valid sharers' rows come out as without it."""
+    step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [4, 9, 30], [],
+                                seed=12)
+    blocks, plen, sharers = step.shared_prefix
+    good = StepRun(step).run(kinds=("decode",), share_prefix=True)["out_decode"]
+    assert pa.get_status() == 0
+    for bad in (step.decode.num_seqs + 3, -1):
+        with_bad = np.concatenate([sharers, [bad]]).astype(np.int32)
+        run = StepRun(W.replace(step, shared_prefix=(blocks, plen, with_bad)))
+        out = run.run(kinds=("decode",), share_prefix=True)["out_decode"]
+        assert pa.get_status() & pa.STATUS_BAD_CONTEXT
+        assert torch.equal(out, good)
+
+
 def test_rejects_bad_arguments(pa):
     step = W.shared_prefix_step("sp", W.Shape(32, 8, 128, 16, "bf16"), 256, [4, 9], [], seed=1)
     run = StepRun(step)
