@@ -59,6 +59,10 @@ struct DecodeParams {
   int out_bytes;   // bytes per output element
   int out_bf16;    // output is bf16
   float scale_log2;
+  // the caches, for L2 prefetches of the first partitions' K/V while the plan is built
+  const void* k_cache;
+  const void* v_cache;
+  long long prefetch_bytes;  // at most this many bytes prefetched (0: none)
 };
 
 // A unit as the producer hands it to its consumer.
@@ -67,6 +71,18 @@ struct UnitDesc {
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// Tokens per split-KV partition for a batch of `total` context tokens: about kTargetUnits
+// (partition, KV head) units, whole blocks, within [kMinPartBlocks, kMaxPartBlocks] blocks.
+// The plan kernel sets the partitions with it, and the attention kernel recomputes it to
+// predict the plan's first units.
+__device__ __forceinline__ int partition_tokens(long long total, int num_kv_heads, int block_size) {
+  long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
+  want = (want + block_size - 1) / block_size * block_size;
+  want = max(want, (long long)kMinPartBlocks * block_size);
+  want = min(want, (long long)kMaxPartBlocks * block_size);
+  return (int)want;
+}
 
 // ----------------------------------------------------------------------------------
 // 1. plan
@@ -96,7 +112,8 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   if (!wait_late) griddep_wait();
   griddep_launch_dependents();
   __shared__ long long s_sum[32];
-  __shared__ int s_off[32];
+  __shared__ int s_off[32], s_foff[32];
+  __shared__ int s_ftotal;
   __shared__ int s_hist[kMaxPartBlocks + 2];
   __shared__ int s_psz, s_total, s_units, s_nmerge;
   // each sequence's own context (past a shared prefix), read once from memory: the later
@@ -147,13 +164,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     long long total = lane < nwarps ? s_sum[lane] : 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(~0u, total, o);
-    if (lane == 0) {
-      long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
-      want = (want + block_size - 1) / block_size * block_size;
-      want = max(want, (long long)kMinPartBlocks * block_size);
-      want = min(want, (long long)kMaxPartBlocks * block_size);
-      s_psz = (int)want;
-    }
+    if (lane == 0) s_psz = partition_tokens(total, num_kv_heads, block_size);
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
@@ -185,6 +196,16 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     warp_claim(s_hist, tail_bucket(c, np), lane);
     full += np > 1 ? np - 1 : 0;
   }
+  // full partitions take the first slots of the list in sequence order (so that the
+  // attention kernel can predict them): each thread's offset is an exclusive scan of the
+  // full-partition counts over threads, which own consecutive sequences
+  const int flocal = full;
+  int fincl = flocal;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(~0u, fincl, o);
+    if (lane >= o) fincl += v;
+  }
 #pragma unroll
   for (int o = 16; o; o >>= 1) full += __shfl_xor_sync(~0u, full, o);
   if (lane == 0 && full > 0) atomicAdd(&s_hist[bpp], full);
@@ -194,18 +215,32 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     const int v = __shfl_up_sync(~0u, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) s_off[wid] = incl;
+  if (lane == 31) {
+    s_off[wid] = incl;
+    s_foff[wid] = fincl;
+  }
   __syncthreads();
   if (wid == 0) {
     const int v = lane < nwarps ? s_off[lane] : 0;
-    int iv = v;
+    const int fv = lane < nwarps ? s_foff[lane] : 0;
+    int iv = v, ifv = fv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(~0u, iv, o);
-      if (lane >= o) iv += t;
+      const int ft = __shfl_up_sync(~0u, ifv, o);
+      if (lane >= o) {
+        iv += t;
+        ifv += ft;
+      }
     }
-    if (lane < nwarps) s_off[lane] = iv - v;
-    if (lane == 31) s_total = iv;
+    if (lane < nwarps) {
+      s_off[lane] = iv - v;
+      s_foff[lane] = ifv - fv;
+    }
+    if (lane == 31) {
+      s_total = iv;
+      s_ftotal = ifv;
+    }
   }
   __syncthreads();
   int run = s_off[wid] + incl - local;
@@ -239,12 +274,15 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
       off += v[k];
     }
     if (lane == 31) s_units = incl;  // partitions with a K/V range of their own
+    // the largest bucket (offset 0) starts with every full partition, placed below; last
+    // partitions of that size are claimed after them
+    if (lane == 0) s_hist[bpp] += s_ftotal;
   }
   __syncthreads();
-  // Placement pass: a sequence's np - 1 full partitions take consecutive slots of the
-  // largest bucket (a warp scan of the counts and one atomic per warp), its last one a
-  // slot of its own bucket.
+  // Placement pass: a sequence's np - 1 full partitions take consecutive slots after those
+  // of the sequences before it, its last one a slot of its own bucket.
   run = s_off[wid] + incl - local;
+  int frun = s_foff[wid] + fincl - flocal;
   for (int i = 0; i < per; ++i) {
     const int b = b0 + i;
     int c = 0, st = 0, rs = 0, np = 0;
@@ -254,16 +292,8 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
       rs = reserved_of(b);
       np = (c + psz - 1) / psz;
     }
-    const int nfull = np > 1 ? np - 1 : 0;
-    int fincl = nfull;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(~0u, fincl, o);
-      if (lane >= o) fincl += t;
-    }
-    int fbase = 0;
-    if (lane == 31 && fincl > 0) fbase = atomicAdd(&s_hist[bpp], fincl);
-    fbase = __shfl_sync(~0u, fbase, 31) + fincl - nfull;
+    const int fbase = frun;
+    frun += np > 1 ? np - 1 : 0;
     const int tslot = warp_claim(s_hist, tail_bucket(c, np), lane);
     for (int p = 0; p < np; ++p) {
       const int ntok = min(psz, c - p * psz);
@@ -699,6 +729,94 @@ __device__ __forceinline__ void consume_t(const DecodeParams& p, UnitDesc* mydes
   }
 }
 
+// Sequences up to which the attention kernel predicts the plan's first units, and the
+// bytes of those units' K/V it brings into L2 meanwhile (about what HBM moves while the
+// plan is built).
+constexpr int kPrefetchMaxSeqs = 4096;
+constexpr long long kDecodePrefetchBytes = 48ll << 20;
+
+// While the plan is being built, brings into L2 the K/V of the first units the attention
+// kernel will take: the plan puts every sequence's full partitions first, in sequence
+// order, with a partition size that depends only on the clamped context lengths, so each
+// CTA recomputes both from the lengths (in `scratch`, 2 * kPrefetchMaxSeqs + 64 ints of
+// shared memory) and its threads spread the first prefetch_bytes of those units over the
+// grid, one block of one unit at a time.  Hints only: what the kernel computes does not depend on them.  Every thread of
+// the CTA calls it.
+template <typename T, int D, int BS, int NT>
+__device__ void prefetch_first_units(const DecodeParams& p, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = p.num_seqs, hkv = p.num_kv_heads;
+  int* s_c = scratch;                          // clamped context length of each sequence
+  int* s_f = scratch + kPrefetchMaxSeqs;       // its first full partition's index
+  long long* s_red = reinterpret_cast<long long*>(scratch + 2 * kPrefetchMaxSeqs);
+  int* s_w = scratch + 2 * kPrefetchMaxSeqs + 2 * (NT / 32);
+  long long tot = 0;
+  for (int b = tid; b < n; b += NT) {
+    const int c = clamp_ctx(__ldcg(p.context_lens + b), p.ctx_cap);
+    s_c[b] = c;
+    tot += c;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(~0u, tot, o);
+  if (lane == 0) s_red[wid] = tot;
+  __syncthreads();
+  long long total = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) total += s_red[w];
+  const int psz = partition_tokens(total, hkv, BS), bpp = psz / BS;
+  auto nfull = [&](int c) { return c > psz ? (c + psz - 1) / psz - 1 : 0; };
+  const int per = (n + NT - 1) / NT, b0 = min(n, tid * per), b1 = min(n, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += nfull(s_c[b]);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_w[wid] = incl;
+  __syncthreads();
+  int off = incl - sum, ftotal = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    if (w < wid) off += s_w[w];
+    ftotal += s_w[w];
+  }
+  for (int b = b0; b < b1; ++b) {
+    s_f[b] = off;
+    off += nfull(s_c[b]);
+  }
+  __syncthreads();
+  constexpr uint32_t kSlice = BS * D * sizeof(T);  // one block of one head, K or V
+  const long long unit_bytes = 2ll * bpp * kSlice;
+  const long long units = min((long long)ftotal * hkv, p.prefetch_bytes / unit_bytes);
+  const T* kc = static_cast<const T*>(p.k_cache);
+  const T* vc = static_cast<const T*>(p.v_cache);
+  // one (unit, block) pair per thread at a time, spread over the whole grid (each SM's
+  // bulk-copy engine also serves its own K/V loads)
+  const long long pairs = units * bpp, stride = (long long)gridDim.x * NT;
+  for (long long f = (long long)blockIdx.x * NT + tid; f < pairs; f += stride) {
+    const long long u = f / bpp;
+    const int i = (int)(f - u * bpp);
+    const int q = (int)(u / hkv), h = (int)(u - (long long)q * hkv);
+    int lo = 0, hi = n;  // the last sequence whose first full partition is <= q
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_f[mid] <= q) lo = mid + 1;
+      else hi = mid;
+    }
+    const int b = lo - 1;
+    const int bi = (q - s_f[b]) * bpp + i;
+    if (bi >= p.max_blocks) continue;
+    const int id = __ldg(p.block_tables + (size_t)b * p.max_blocks + bi);
+    if (id < 0 || id >= p.num_blocks) continue;
+    const size_t e = ((size_t)id * hkv + h) * BS * D;
+    prefetch_l2_bulk(kc + e, kSlice);
+    prefetch_l2_bulk(vc + e, kSlice);
+  }
+  __syncthreads();  // the scratch is the K/V ring from here on
+}
+
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -736,6 +854,8 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  if (p.prefetch_bytes > 0 && p.num_seqs <= kPrefetchMaxSeqs)
+    prefetch_first_units<T, D, BS, C::kThreads>(p, reinterpret_cast<int*>(stages));
   __syncthreads();
   griddep_wait();  // the plan kernel's work list is complete from here on
 
@@ -1289,6 +1409,11 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.out_bytes = (int)dtype_bytes(a.out_dtype);
   p.out_bf16 = a.out_dtype == PA_BF16;
   p.scale_log2 = a.scale * kLog2e;
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
+  // the first partitions' K/V that HBM can bring in while the plan is built (not with a
+  // shared prefix, whose sequences' partitions start after it)
+  p.prefetch_bytes = a.prefix.num_sharers > 0 ? 0 : kDecodePrefetchBytes;
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {
