@@ -63,6 +63,10 @@ struct DecodeParams {
   const void* k_cache;
   const void* v_cache;
   long long prefetch_bytes;  // at most this many bytes prefetched (0: none)
+  // The attention kernel waits for the plan through the workspace flag (header[5], set
+  // by the plan once its list is written) rather than through the launch dependency, and
+  // for the kernel launched just before it (the shared prefix's) only before it exits.
+  int plan_flag;
 };
 
 // A unit as the producer hands it to its consumer.
@@ -110,6 +114,12 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   // writes; it is waited for only at the end, so that the work list is built meanwhile
   // and the next kernel still starts after both (lengths are read through L2)
   if (!wait_late) griddep_wait();
+  // with a shared prefix the attention kernel waits for the flag this kernel sets at its
+  // end: cleared before the kernels after this one may launch
+  if (pre.num_sharers > 0 && threadIdx.x == 0) {
+    ws.header[5] = 0;
+    __threadfence();
+  }
   griddep_launch_dependents();
   __shared__ long long s_sum[32];
   __shared__ int s_off[32], s_foff[32];
@@ -318,12 +328,17 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     ws.header[4] = s_nmerge;
   }
   if (wait_late) griddep_wait();
+  if (pre.num_sharers > 0) {
+    __threadfence();  // every thread's writes, before the flag
+    __syncthreads();
+    if (tid == 0) atomicExch(ws.header + 5, 1);
+  }
 }
 
 // A unit is (partition, KV head): unit u is partition u / H_kv for KV head u % H_kv.
 __device__ __forceinline__ PartRec load_part(const DecodeParams& p, int u) {
   const int4* src = reinterpret_cast<const int4*>(p.ws.parts + u / p.num_kv_heads);
-  const int4 a = __ldg(src), c = __ldg(src + 1);
+  const int4 a = __ldcg(src), c = __ldcg(src + 1);  // written by the plan kernel
   PartRec r;
   r.b = a.x; r.p = a.y; r.tok0 = a.z; r.ntok = a.w;
   r.part_start = c.x; r.nparts = c.y; r.pad0 = c.z; r.pad1 = c.w;
@@ -854,12 +869,37 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  static_assert((size_t)C::kPairs * S * C::kStageBytes >= (2 * kPrefetchMaxSeqs + 64) * 4,
+                "the prefetch scratch fits in the K/V rings");
   if (p.prefetch_bytes > 0 && p.num_seqs <= kPrefetchMaxSeqs)
     prefetch_first_units<T, D, BS, C::kThreads>(p, reinterpret_cast<int*>(stages));
-  __syncthreads();
-  griddep_wait();  // the plan kernel's work list is complete from here on
-
-  const int total_units = p.ws.header[1];
+  // with plan_flag set, every thread waits for the kernel launched before this one (the
+  // shared prefix's) on its way out, so that this grid ends after it and the merge,
+  // which waits for this grid, also waits for it
+  struct WaitAtExit {
+    int on;
+    __device__ ~WaitAtExit() {
+      if (on) griddep_wait();
+    }
+  } wait_at_exit{p.plan_flag};
+  __shared__ int s_plan_ready;
+  if (p.plan_flag) {
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = global_timer_ns();
+      int v;
+      while ((v = ld_acquire_gpu(p.ws.header + 5)) == 0 &&
+             global_timer_ns() - t0 < kWaitTimeoutNs)
+        __nanosleep(128);
+      s_plan_ready = v;
+      if (v == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
+    }
+    __syncthreads();
+  } else {
+    __syncthreads();
+    griddep_wait();  // the plan kernel's work list is complete from here on
+  }
+  // (a plan that never finished leaves no work: the kernel only waits and exits)
+  const int total_units = !p.plan_flag || s_plan_ready ? __ldcg(p.ws.header + 1) : 0;
 
   if (warp >= C::kPairs) {
     // ------------------------------ producer warp ------------------------------
@@ -1362,7 +1402,10 @@ PrefixPlan plan_prefix(int num_sharers, int prefix_len, int group, int num_kv_he
     pp.splits = 0;
     return pp;
   }
-  constexpr int kTile = 128, kRowsPerCta = 256, kTargetCtas = 152;  // one wave
+  // about a third of the SMs (here 48 of 152): the attention over the sequences' own
+  // contexts takes the others meanwhile (a constant, so that the workspace size does
+  // not depend on the device)
+  constexpr int kTile = 128, kRowsPerCta = 256, kTargetCtas = 48;
   const long long row_ctas = ((long long)num_sharers * group + kRowsPerCta - 1) / kRowsPerCta;
   const long long tiles = (prefix_len + kTile - 1) / kTile;
   long long want = (kTargetCtas + row_ctas * num_kv_heads - 1) / (row_ctas * num_kv_heads);
@@ -1414,6 +1457,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // the first partitions' K/V that HBM can bring in while the plan is built (not with a
   // shared prefix, whose sequences' partitions start after it)
   p.prefetch_bytes = a.prefix.num_sharers > 0 ? 0 : kDecodePrefetchBytes;
+  p.plan_flag = a.prefix.num_sharers > 0;
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {

@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(384, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // the attention kernel, launched next, waits for the plan through a flag of its own and
+  // for this grid only on its way out: it may start now, on the SMs this grid leaves free
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   bool valid[NT];
 #pragma unroll
