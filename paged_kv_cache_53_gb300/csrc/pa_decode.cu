@@ -922,9 +922,14 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
         griddep_launch_dependents();
         break;
       }
-      if (lane == 0) next_u = atomicAdd(p.ws.header, 1);  // claim the next unit early
       const UnitDesc d = describe_unit(load_part(p, u), u, p.num_kv_heads);
       const int ntiles = (d.ntok + BS - 1) / BS;
+      // The next unit is claimed when about a ring's worth of this unit's tiles is left to
+      // issue: early enough to load its record and block list while those are consumed,
+      // late enough that near the end of the list no unit waits behind a busy pair while
+      // others have run out.
+      const int claim_at = ntiles > S ? ntiles - S : 0;
+      if (ntiles == 0 && lane == 0) next_u = atomicAdd(p.ws.header, 1);
       const int32_t* row = p.block_tables + (size_t)d.b * p.max_blocks + d.tok0 / BS;
       int ids[kMaxPartBlocks / 32];
 #pragma unroll
@@ -950,6 +955,7 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
       }
       ++q_it;
       for (int t = 0; t < ntiles; ++t) {
+        if (t == claim_at && lane == 0) next_u = atomicAdd(p.ws.header, 1);
         const int s = tile_it % S;
         if (!mbar_wait(smem_addr(empty + s), ((tile_it / S) & 1) ^ 1)) { ok = false; break; }
         const int k = t >> 5;
