@@ -41,6 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context; the roofline uses the measured copy)
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_53_gb300", "csrc", "pa_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+# end-to-end pass: steps shorter than this replay a captured CUDA graph (see run_ours)
+GRAPH_STEP_MS = 0.1
 
 
 # ------------------------------------------------------------------ accounting
@@ -441,10 +443,14 @@ def run_ours(args, rank, world, local_rank):
             d_bufs[bi].copy_(h_buf, non_blocking=True)
             ready[bi].record(copy_stream)
 
-    # the step's launches captured once per buffer set and replayed every step (inputs
-    # are read from the buffers at replay time), so that the host keeps ahead of short steps
+    # Steps shorter than GRAPH_STEP_MS: the step's launches captured once per buffer set and
+    # replayed every step (inputs are read from the buffers at replay time), so that the
+    # host keeps ahead of them.  Longer steps are launched directly: each graph replay
+    # starts only once the previous one has ended, where direct launches let the next
+    # step's first kernel be set up while the previous one finishes.
     graphs = []
-    if not args.no_graphs:
+    use_graphs = args.graphs == "on" or (args.graphs == "auto" and total_ms / k < GRAPH_STEP_MS)
+    if use_graphs:
         for bi in range(2):
             d_bufs[bi].copy_(h_buf)
             one_step(io=d_io[bi])  # the library's one-time set-up happens outside capture
@@ -922,9 +928,10 @@ def main():
                     help="step: the hot path over --workload; swap: pa_swap_blocks bandwidth; "
                          "blockmgr: host block-manager time per decode step")
     ap.add_argument("--swap-blocks", type=int, default=8192)
-    ap.add_argument("--no-graphs", action="store_true",
-                    help="issue the end-to-end steps' launches from the host instead of "
-                         "replaying a captured CUDA graph")
+    ap.add_argument("--graphs", choices=["auto", "on", "off"], default="auto",
+                    help="end-to-end steps: replay a captured CUDA graph (on), issue the "
+                         "launches from the host (off), or graphs only for steps shorter "
+                         "than %.2f ms (auto)" % GRAPH_STEP_MS)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
