@@ -21,8 +21,13 @@
  * Memory.  Every pointer argument named *_cache, q, out, k_new, v_new, block_tables,
  *   context_lens, cu_q_lens, slot_mapping, pairs and workspace is a DEVICE pointer
  *   owned by the caller and must be 16-byte aligned.  The library allocates no device
- *   memory and keeps no state between calls except a per-device status word (and the
- *   fixed scratch array of pa_decode_static_scratch).
+ *   memory.  What it keeps between calls: a status word per device, the table of
+ *   caller-owned status words (pa_set_stream_status), the fixed scratch array of
+ *   pa_decode_static_scratch, per-device handles it looks up once (the device
+ *   addresses of that word and array, SM counts, kernel attributes), and the stream and
+ *   two events pa_mixed_step creates per device and host thread (freed by
+ *   pa_release_thread_resources).  cudaDeviceReset invalidates those handles: do not
+ *   call the library on a device after resetting it in the same process.
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
  *   enqueues work on it and returns without synchronising.
  * Errors.  A call returns PA_OK or a PA_ERR_* code.  Arguments are validated on the
@@ -30,7 +35,8 @@
  *   pa_last_error_string() (thread-local) says why.  Data-dependent faults found by the
  *   kernels (a block id outside the pool, a slot outside the pool, a context longer
  *   than its table) never trap: the offending access is skipped or reads zeros, and a
- *   bit is set in the device status word read by pa_get_status().
+ *   bit is set in the device status word read by pa_get_status() (or in the word the
+ *   caller gave the call's stream with pa_set_stream_status).
  * Supported shapes.  head_dim in {64, 128}; block_size in {16, 32};
  *   num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.  dtype PA_F32, PA_F16, PA_BF16 for
  *   cache writes, copies and decode; PA_F16 and PA_BF16 for chunked prefill.
@@ -70,15 +76,44 @@ int pa_version(void);
 const char* pa_last_error_string(void);
 
 /* Reads the current device's status word into *status and clears it.  Synchronises
- * the device.  Returns PA_ERR_CUDA if the device cannot be reached. */
+ * the device.  Returns PA_ERR_CUDA if the device cannot be reached.  Bits of calls on a
+ * stream with a word of its own (pa_set_stream_status) do not appear here. */
 int pa_get_status(int32_t* status);
+
+/*
+ * pa_set_stream_status -- gives the calls on one stream a status word of their own.
+ *
+ * The device-wide word read by pa_get_status() is shared by every caller on the device,
+ * and reading it clears the bits of all of them.  After this call, the kernels of every
+ * call enqueued on `stream` (a cudaStream_t of the current device; NULL = the legacy
+ * default stream) OR their PA_STATUS_* bits into `*status` instead: an int32 in DEVICE
+ * memory, 4-byte aligned, owned by the caller, which the library never reads or clears
+ * (the caller reads and zeroes it, e.g. with cudaMemcpyAsync / cudaMemsetAsync on the
+ * same stream).  Registering a stream again replaces its word; status = NULL removes the
+ * stream's entry.  Remove it before destroying the stream (a later stream may get the
+ * same handle).  A call enqueued on a stream picks its word when it is made.  The work
+ * pa_mixed_step runs on its own stream reports to the word of the caller's `stream`.
+ * At most 64 (device, stream) entries exist at a time: PA_ERR_UNSUPPORTED beyond.
+ * Returns PA_ERR_INVALID_ARG for a misaligned word, PA_ERR_CUDA without a device.
+ */
+int pa_set_stream_status(void* stream, int32_t* status);
+
+/*
+ * pa_release_thread_resources -- destroys the stream and the two events pa_mixed_step
+ * created for the calling host thread (one set per device it ran on).  Call it before a
+ * thread that used pa_mixed_step exits, or whenever it is done with the library; a later
+ * pa_mixed_step creates them again.  No work of the thread's pa_mixed_step calls may
+ * still be pending when it is called (synchronise their streams first).  Returns
+ * PA_ERR_CUDA if a handle could not be destroyed (the others are destroyed regardless).
+ */
+int pa_release_thread_resources(void);
 
 /* Self-test of the kernels' bounded waits: launches one CTA on `stream` (cudaStream_t,
  * may be null) that waits on a shared-memory mbarrier nothing ever arrives on, with the
  * wait function every pipeline in this library uses, given up after `timeout_us`
  * microseconds (1 .. 2,000,000) instead of the library's 2 s.  The kernel then sets
- * PA_STATUS_TIMEOUT in the status word and returns: the device stays usable, and
- * pa_get_status() reports the bit.  No other effect.  Returns PA_ERR_INVALID_ARG for a
+ * PA_STATUS_TIMEOUT in the status word (the stream's own word if it has one) and returns:
+ * the device stays usable, and pa_get_status() reports the bit.  No other effect.  Returns PA_ERR_INVALID_ARG for a
  * timeout out of range, PA_ERR_CUDA if the launch fails. */
 int pa_selftest_wait_timeout(int timeout_us, void* stream);
 
@@ -299,7 +334,9 @@ int pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, const 
  *            sequences of up to 131072 tokens do not).
  *   Memory.  Every GPU that loads the library reserves the 32 MiB until the process
  *            exits.  The first call on each device looks up the array's device address
- *            (cudaGetSymbolAddress); make that first call before any stream capture.
+ *            (cudaGetSymbolAddress) and keeps it for the later calls; make that first
+ *            call before any stream capture.  A device reset invalidates the kept address
+ *            (see "Memory" above: do not use the library after cudaDeviceReset).
  *   Sharing. All calls on a device share the one array and it keeps the last call's
  *            contents; each call rewrites what it reads, so nothing has to be cleared
  *            between calls.  Calls that overlap in time on the GPU (different streams,
@@ -338,8 +375,9 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int n
  *   workspace     device scratch of pa_prefill_workspace_bytes(...) bytes (may be 0)
  * QK^T and PV run on the tensor cores with fp32 accumulation.  P and V enter the PV
  * product in fp16 (unit roundoff 2^-11; bf16's 2^-8 alone would not meet a 2e-3 bound):
- * bf16 V values are converted to fp16 in shared memory, which is exact below 65520 in
- * magnitude; a larger V value sets PA_STATUS_RANGE (its products are not exact).
+ * bf16 V values are converted to fp16 in shared memory, which is exact for magnitudes
+ * from 2^-14 up to 65520 (below 2^-14 they become fp16 subnormals, within 2^-25); a V
+ * value of 65520 or more sets PA_STATUS_RANGE (its products are not exact).
  */
 int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
                      const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
@@ -362,7 +400,9 @@ int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k
  * kernel on about 58% of the SMs; the prefill runs on a stream of the library's own that
  * waits for the work enqueued on `stream` before the call, and `stream` waits for it
  * before any later work (so the call is stream-ordered as usual, under graph capture
- * too).  The two batches must not share sequences.
+ * too).  That stream and its two events are created on the first call per device and
+ * host thread and kept for the next ones; pa_release_thread_resources destroys them.
+ * The two batches must not share sequences.
  *
  *   dec   the decode batch: one new token per sequence (row b of k_new / v_new), as in
  *         pa_decode_append; null or num_seqs = 0 for none

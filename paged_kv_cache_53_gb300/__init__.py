@@ -25,6 +25,8 @@ __all__ = [
     "decode_workspace_bytes",
     "decode", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
     "prefill_workspace_bytes", "prefill_chunk", "get_status", "version",
+    "set_stream_status", "release_thread_resources",
+    "testing_decode_workspace_bytes", "testing_decode_partitions",
     "STATUS_BAD_BLOCK", "STATUS_BAD_SLOT", "STATUS_BAD_CONTEXT", "STATUS_TIMEOUT", "STATUS_RANGE",
 ]
 
@@ -52,6 +54,11 @@ _SIGNATURES = {
     "pa_version": ([], _i),
     "pa_last_error_string": ([], ctypes.c_char_p),
     "pa_get_status": ([_p], _i),
+    "pa_set_stream_status": ([_p, _p], _i),
+    "pa_release_thread_resources": ([], _i),
+    "pa_testing_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "pa_testing_decode_partitions": ([_p, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i,
+                                      _i, _f, _i, _i, _p, _sz, _p], _i),
     "pa_selftest_wait_timeout": ([_i, _p], _i),
     "pa_mixed_step": ([_p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _i, _p], _i),
     "pa_slot_mapping": ([_p, _p, _i, _p, _p, _i, _i, _i, _i, _p], _i),
@@ -341,6 +348,44 @@ def prefill_chunk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                                   _ptr(cu_q_lens), _ptr(context_lens), context_lens.shape[0], t,
                                   max_q, max_ctx, h_q, h_kv, d, bs, nb, float(scale),
                                   dtype_code(k_cache.dtype), ws_ptr, ws_bytes, _stream(stream)))
+
+
+def testing_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                   head_dim: int, max_ctx: int, block_size: int,
+                                   part_blocks: int) -> int:
+    return int(lib().pa_testing_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                       head_dim, max_ctx, block_size,
+                                                       part_blocks))
+
+
+def testing_decode_partitions(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                              v_cache: torch.Tensor, block_tables: torch.Tensor,
+                              context_lens: torch.Tensor, max_ctx: int, scale: float,
+                              part_blocks: int, workspace: torch.Tensor, stream=None):
+    """pa_decode with every context cut into partitions of `part_blocks` blocks (see
+    pa_testing_decode_partitions in include/pa_testing.h)."""
+    nb, h_kv, bs, d = k_cache.shape
+    b, h_q, _ = q.shape
+    _check(lib().pa_testing_decode_partitions(
+        _ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), max_ctx, b, h_q, h_kv, d,
+        bs, nb, float(scale), dtype_code(k_cache.dtype), int(part_blocks), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def set_stream_status(stream, status: Optional[torch.Tensor]):
+    """Routes the status bits of calls on `stream` (a torch.cuda.Stream) into `status`, a
+    one-element int32 CUDA tensor the caller reads and clears; None removes the route
+    (see pa_set_stream_status)."""
+    if status is not None:
+        if status.dtype != torch.int32 or status.device.type != "cuda" or status.numel() < 1:
+            raise TypeError("status must be an int32 CUDA tensor")
+    _check(lib().pa_set_stream_status(_stream(stream), _ptr(status)))
+
+
+def release_thread_resources():
+    """Destroys the side stream and events pa_mixed_step created for this thread."""
+    _check(lib().pa_release_thread_resources())
 
 
 def get_status() -> int:

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -10,6 +11,7 @@
 
 #include "pa.h"
 #include "pa_device.cuh"
+#include "pa_testing.h"
 #include "pa_internal.h"
 
 namespace pa {
@@ -24,6 +26,17 @@ __device__ int32_t g_status_word;  // one per device that loads the library
 int32_t* g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::mutex g_mutex;
+
+// Caller-owned status words registered per (device, stream) by pa_set_stream_status.
+struct StreamStatus {
+  int dev;
+  cudaStream_t stream;
+  int32_t* word;
+};
+constexpr int kMaxStreamStatus = 64;
+StreamStatus g_stream_status[kMaxStreamStatus];
+int g_num_stream_status = 0;                 // entries in use (under g_mutex)
+std::atomic<int> g_stream_status_used{0};    // the same count, read without the lock
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -105,7 +118,7 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
-int32_t* status_word() {
+int32_t* device_status_word() {
   const int dev = current_device();
   if (dev < 0) return nullptr;
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -115,6 +128,18 @@ int32_t* status_word() {
     g_status_ptr[dev] = static_cast<int32_t*>(p);
   }
   return g_status_ptr[dev];
+}
+
+int32_t* status_word(void* stream) {
+  if (g_stream_status_used.load(std::memory_order_acquire) > 0) {
+    const int dev = current_device();
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (int i = 0; i < g_num_stream_status; ++i)
+      if (g_stream_status[i].dev == dev && g_stream_status[i].stream == s)
+        return g_stream_status[i].word;
+  }
+  return device_status_word();
 }
 
 int sm_count() {
@@ -189,7 +214,7 @@ int pa_selftest_wait_timeout(int timeout_us, void* stream) {
   if (timeout_us < 1 || timeout_us > 2000000)
     return pa::fail(PA_ERR_INVALID_ARG, "pa_selftest_wait_timeout: timeout_us %d outside [1, 2e6]",
                     timeout_us);
-  int32_t* st = pa::status_word();
+  int32_t* st = pa::status_word(stream);
   if (st == nullptr) return pa::fail(PA_ERR_CUDA, "pa_selftest_wait_timeout: no usable device");
   const cudaError_t e = pa::launch_selftest_wait((uint64_t)timeout_us * 1000ull, st,
                                                   static_cast<cudaStream_t>(stream));
@@ -198,10 +223,38 @@ int pa_selftest_wait_timeout(int timeout_us, void* stream) {
   return PA_OK;
 }
 
+int pa_set_stream_status(void* stream, int32_t* status) {
+  g_error[0] = '\0';
+  const int dev = current_device();
+  if (dev < 0) return fail(PA_ERR_CUDA, "pa_set_stream_status: no usable CUDA device");
+  if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "pa_set_stream_status: status word must be 4-byte aligned");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int found = -1;
+  for (int i = 0; i < g_num_stream_status; ++i)
+    if (g_stream_status[i].dev == dev && g_stream_status[i].stream == s) found = i;
+  if (status == nullptr) {  // remove the entry (keeping the others packed)
+    if (found >= 0) {
+      g_stream_status[found] = g_stream_status[g_num_stream_status - 1];
+      --g_num_stream_status;
+    }
+  } else if (found >= 0) {
+    g_stream_status[found].word = status;
+  } else {
+    if (g_num_stream_status == kMaxStreamStatus)
+      return fail(PA_ERR_UNSUPPORTED, "pa_set_stream_status: more than %d streams registered",
+                  kMaxStreamStatus);
+    g_stream_status[g_num_stream_status++] = StreamStatus{dev, s, status};
+  }
+  g_stream_status_used.store(g_num_stream_status, std::memory_order_release);
+  return PA_OK;
+}
+
 int pa_get_status(int32_t* status) {
   g_error[0] = '\0';
   if (status == nullptr) return fail(PA_ERR_INVALID_ARG, "pa_get_status: null output pointer");
-  int32_t* p = status_word();
+  int32_t* p = device_status_word();
   if (p == nullptr) return fail(PA_ERR_CUDA, "pa_get_status: no usable CUDA device");
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(status, p, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
@@ -222,7 +275,7 @@ int pa_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks_
     return fail(PA_ERR_INVALID_ARG, "pa_slot_mapping: tokens without sequences or blocks");
   if (!slots || !block_tables || !cu_q_lens || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "pa_slot_mapping: null pointer");
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_slot_mapping: no usable CUDA device");
   cudaError_t e = launch_slot_mapping(slots, block_tables, max_blocks_per_seq, cu_q_lens,
                                       context_lens, num_seqs, num_tokens, block_size, num_blocks,
@@ -245,7 +298,7 @@ int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, vo
     return fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: null pointer");
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: K/V pointers must be 16-byte aligned");
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_reshape_and_cache: no usable CUDA device");
   cudaError_t e = launch_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
                                            num_tokens, num_kv_heads, head_dim, block_size,
@@ -274,7 +327,7 @@ int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v
     return fail(PA_ERR_INVALID_ARG, "pa_cache_append: null pointer");
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PA_ERR_INVALID_ARG, "pa_cache_append: K/V pointers must be 16-byte aligned");
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_cache_append: no usable CUDA device");
   cudaError_t e = launch_cache_append(k_new, v_new, k_cache, v_cache, slots, block_tables,
                                       max_blocks_per_seq, cu_q_lens, context_lens, num_seqs,
@@ -304,7 +357,7 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
       return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: layer %d cache pointer null or unaligned",
                   l);
   }
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_copy_blocks: no usable CUDA device");
   const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * dtype_bytes(dtype);
   cudaError_t e = launch_copy_blocks(k_caches, v_caches, num_layers, pairs, num_pairs,
@@ -332,7 +385,7 @@ int pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
     return fail(PA_ERR_UNSUPPORTED, "pa_swap_blocks: %d layers > %d", num_layers, kMaxSwapLayers);
   if (!src_k || !src_v || !dst_k || !dst_v || !pairs)
     return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: null pointer");
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_swap_blocks: no usable CUDA device");
   void* views[4][kMaxSwapLayers];
   void* const* in[4] = {src_k, src_v, dst_k, dst_v};
@@ -377,7 +430,7 @@ static int decode_args(const char* who, void* out, pa_dtype out_dtype, const voi
                        int max_blocks_per_seq, const int32_t* context_lens, int max_ctx,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int block_size, int num_blocks, float scale, pa_dtype dtype,
-                       void* workspace, size_t workspace_bytes, DecodeArgs& a) {
+                       void* workspace, size_t workspace_bytes, void* stream, DecodeArgs& a) {
   int rc = check_cache_geometry(who, num_kv_heads, head_dim, block_size, num_blocks, dtype);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || max_ctx < 0 || num_q_heads <= 0)
@@ -402,7 +455,7 @@ static int decode_args(const char* who, void* out, pa_dtype out_dtype, const voi
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
                 need);
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
   a.out = out;
   a.out_dtype = out_dtype;
@@ -458,7 +511,7 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
   const int rc = decode_args("pa_decode", out, out_dtype, q, k_cache, v_cache, block_tables,
                              max_blocks_per_seq, context_lens, max_ctx, num_seqs, num_q_heads,
                              num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
-                             workspace, workspace_bytes, a);
+                             workspace, workspace_bytes, stream, a);
   if (rc != PA_OK) return rc;
   return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
@@ -482,7 +535,7 @@ int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k
   int rc = decode_args("pa_decode_append", out, out_dtype, q, k_cache, v_cache, block_tables,
                        max_blocks_per_seq, context_lens, max_ctx, num_seqs, num_q_heads,
                        num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
-                       workspace_bytes, a);
+                       workspace_bytes, stream, a);
   if (rc != PA_OK) return rc;
   return launch_decode_append("pa_decode_append", a, k_new, v_new, slots,
                               static_cast<cudaStream_t>(stream));
@@ -549,7 +602,7 @@ int pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, const 
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE, "pa_decode_shared_prefix: workspace %zu bytes < %zu needed",
                 workspace_bytes, need);
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "pa_decode_shared_prefix: no usable CUDA device");
   DecodeArgs a;
   a.out = out;
@@ -578,6 +631,49 @@ int pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, const 
   return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t pa_testing_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int max_ctx, int block_size,
+                                         int part_blocks) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_ctx < 0 ||
+      block_size <= 0 || part_blocks < 1 || part_blocks > kMaxPartBlocks)
+    return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size, 0, part_blocks * block_size);
+}
+
+int pa_testing_decode_partitions(void* out, pa_dtype out_dtype, const void* q,
+                                 const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int max_ctx, int num_seqs,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, float scale, pa_dtype dtype, int part_blocks,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  g_error[0] = '\0';
+  const char* who = "pa_testing_decode_partitions";
+  if (part_blocks < 1 || part_blocks > kMaxPartBlocks)
+    return fail(PA_ERR_INVALID_ARG, "%s: part_blocks %d outside [1, %d]", who, part_blocks,
+                kMaxPartBlocks);
+  if (num_seqs == 0) return PA_OK;
+  // the plain checks with the default workspace size, then the forced size's own
+  DecodeArgs a;
+  const size_t need = pa_testing_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                        head_dim, max_ctx, block_size,
+                                                        part_blocks);
+  if (need == 0) return fail(PA_ERR_INVALID_ARG, "%s: bad sizes", who);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                need);
+  const int rc = decode_args(who, out, out_dtype, q, k_cache, v_cache, block_tables,
+                             max_blocks_per_seq, context_lens, max_ctx, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                             workspace, ~size_t(0), stream, a);
+  if (rc != PA_OK) return rc;
+  a.forced_part_tokens = part_blocks * block_size;
+  a.ws = carve_decode_workspace(workspace, num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                block_size, 0, a.forced_part_tokens);
+  return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int num_q_heads,
                                   int num_kv_heads, int head_dim, int max_ctx, int block_size) {
   if (num_seqs <= 0 || num_tokens < 0 || max_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -597,7 +693,8 @@ static int prefill_args(const char* who, void* out, pa_dtype out_dtype, const vo
                         const int32_t* context_lens, int num_seqs, int num_tokens, int max_q,
                         int max_ctx, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int num_blocks, float scale, pa_dtype dtype,
-                        void* workspace, size_t workspace_bytes, PrefillArgs& a, bool* empty) {
+                        void* workspace, size_t workspace_bytes, void* stream, PrefillArgs& a,
+                        bool* empty) {
   *empty = false;
   int rc = check_cache_geometry(who, num_kv_heads, head_dim, block_size, num_blocks, dtype);
   if (rc != PA_OK) return rc;
@@ -630,7 +727,7 @@ static int prefill_args(const char* who, void* out, pa_dtype out_dtype, const vo
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
                 need);
-  int32_t* st = status_word();
+  int32_t* st = status_word(stream);
   if (st == nullptr) return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
   a.out = out;
   a.out_dtype = out_dtype;
@@ -670,12 +767,13 @@ struct SideStream {
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 
+static thread_local SideStream t_side[64];  // per device, for this host thread
+
 static int side_stream(const char* who, SideStream** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return fail(PA_ERR_CUDA, "%s: no usable CUDA device", who);
-  static thread_local SideStream per_dev[64];
-  SideStream& x = per_dev[dev];
+  SideStream& x = t_side[dev];
   if (x.stream == nullptr) {
     if (cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -712,8 +810,8 @@ int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k
   const int rc = prefill_args("pa_prefill_chunk", out, out_dtype, q, k_cache, v_cache,
                               block_tables, max_blocks_per_seq, cu_q_lens, context_lens, num_seqs,
                               num_tokens, max_q, max_ctx, num_q_heads, num_kv_heads, head_dim,
-                              block_size, num_blocks, scale, dtype, workspace, workspace_bytes, a,
-                              &empty);
+                              block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
+                              stream, a, &empty);
   if (rc != PA_OK || empty) return rc;
   return launch_prefill(a, static_cast<cudaStream_t>(stream));
 }
@@ -739,7 +837,7 @@ int pa_mixed_step(const pa_decode_batch* dec, const pa_prefill_batch* pre, void*
                                dec->block_tables, dec->max_blocks_per_seq, dec->context_lens,
                                dec->max_ctx, dec->num_seqs, num_q_heads, num_kv_heads, head_dim,
                                block_size, num_blocks, scale, dtype, dec->workspace,
-                               dec->workspace_bytes, da);
+                               dec->workspace_bytes, stream, da);
     if (rc != PA_OK) return rc;
   }
   PrefillArgs pa_args;
@@ -750,7 +848,7 @@ int pa_mixed_step(const pa_decode_batch* dec, const pa_prefill_batch* pre, void*
                                 pre->context_lens, pre->num_seqs, pre->num_tokens, pre->max_q,
                                 pre->max_ctx, num_q_heads, num_kv_heads, head_dim, block_size,
                                 num_blocks, scale, dtype, pre->workspace, pre->workspace_bytes,
-                                pa_args, &pre_empty);
+                                stream, pa_args, &pre_empty);
     if (rc != PA_OK) return rc;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -775,6 +873,27 @@ int pa_mixed_step(const pa_decode_batch* dec, const pa_prefill_batch* pre, void*
       cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
     return fail(PA_ERR_CUDA, "%s: %s", who, cudaGetErrorString(cudaGetLastError()));
   return rc != PA_OK ? rc : rc2;
+}
+
+int pa_release_thread_resources(void) {
+  g_error[0] = '\0';
+  int cur = 0;
+  const bool restore = cudaGetDevice(&cur) == cudaSuccess;
+  int rc = PA_OK;
+  for (int dev = 0; dev < 64; ++dev) {
+    SideStream& x = t_side[dev];
+    if (x.stream == nullptr && x.fork == nullptr && x.join == nullptr) continue;
+    // each handle is destroyed with its own device current
+    if (cudaSetDevice(dev) != cudaSuccess ||
+        (x.stream != nullptr && cudaStreamDestroy(x.stream) != cudaSuccess) ||
+        (x.fork != nullptr && cudaEventDestroy(x.fork) != cudaSuccess) ||
+        (x.join != nullptr && cudaEventDestroy(x.join) != cudaSuccess))
+      rc = fail(PA_ERR_CUDA, "pa_release_thread_resources: %s",
+                cudaGetErrorString(cudaGetLastError()));
+    x = SideStream{};
+  }
+  if (restore) cudaSetDevice(cur);
+  return rc;
 }
 
 }  // extern "C"

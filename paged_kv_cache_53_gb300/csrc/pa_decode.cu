@@ -67,6 +67,7 @@ struct DecodeParams {
   // by the plan once its list is written) rather than through the launch dependency, and
   // for the kernel launched just before it (the shared prefix's) only before it exits.
   int plan_flag;
+  int forced_psz;  // partition size set by the caller (tokens), 0: chosen from the batch
 };
 
 // A unit as the producer hands it to its consumer.
@@ -80,7 +81,10 @@ __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c
 // (partition, KV head) units, whole blocks, within [kMinPartBlocks, kMaxPartBlocks] blocks.
 // The plan kernel sets the partitions with it, and the attention kernel recomputes it to
 // predict the plan's first units.
-__device__ __forceinline__ int partition_tokens(long long total, int num_kv_heads, int block_size) {
+// A positive `forced` (whole blocks, set only by the testing entry point) replaces the choice.
+__device__ __forceinline__ int partition_tokens(long long total, int num_kv_heads, int block_size,
+                                                int forced) {
+  if (forced > 0) return forced;
   long long want = (total * num_kv_heads + kTargetUnits - 1) / kTargetUnits;
   want = (want + block_size - 1) / block_size * block_size;
   want = max(want, (long long)kMinPartBlocks * block_size);
@@ -109,7 +113,8 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
                                                            int num_kv_heads, int block_size,
                                                            DecodeWorkspace ws, int32_t* status,
                                                            int4* out, int out_row_vec16,
-                                                           PrefixPlan pre, int wait_late) {
+                                                           PrefixPlan pre, int wait_late,
+                                                           int forced_psz) {
   // wait_late: the previous kernel on the stream writes nothing this kernel reads or
   // writes; it is waited for only at the end, so that the work list is built meanwhile
   // and the next kernel still starts after both (lengths are read through L2)
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     long long total = lane < nwarps ? s_sum[lane] : 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(~0u, total, o);
-    if (lane == 0) s_psz = partition_tokens(total, num_kv_heads, block_size);
+    if (lane == 0) s_psz = partition_tokens(total, num_kv_heads, block_size, forced_psz);
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
@@ -778,7 +783,7 @@ __device__ void prefetch_first_units(const DecodeParams& p, int* scratch) {
   long long total = 0;
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) total += s_red[w];
-  const int psz = partition_tokens(total, hkv, BS), bpp = psz / BS;
+  const int psz = partition_tokens(total, hkv, BS, p.forced_psz), bpp = psz / BS;
   auto nfull = [&](int c) { return c > psz ? (c + psz - 1) / psz - 1 : 0; };
   const int per = (n + NT - 1) / NT, b0 = min(n, tid * per), b1 = min(n, b0 + per);
   int sum = 0;
@@ -1347,7 +1352,11 @@ int launch_mma_dispatch(const DecodeArgs& a, const DecodeParams& p, cudaStream_t
 
 }  // namespace
 
-size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size) {
+size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size,
+                        int forced_psz) {
+  if (forced_psz > 0)
+    return (size_t)((long long)num_seqs * (((long long)max_ctx + forced_psz - 1) / forced_psz) +
+                    num_seqs);
   const long long pmax = (long long)kMaxPartBlocks * block_size;
   const long long by_target = (kTargetUnits + num_kv_heads - 1) / num_kv_heads;
   const long long by_length = (long long)num_seqs * ((max_ctx + pmax - 1) / pmax);
@@ -1359,8 +1368,8 @@ struct WsLayout {
   size_t header, part_start, seq_flags, merge_seqs, units, part_ml, part_acc, total;
 };
 WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
-                       int block_size, long long extra_slots) {
-  const size_t parts = decode_max_parts(num_seqs, num_kv_heads, max_ctx, block_size);
+                       int block_size, long long extra_slots, int forced_psz) {
+  const size_t parts = decode_max_parts(num_seqs, num_kv_heads, max_ctx, block_size, forced_psz);
   const size_t slots = parts + (size_t)extra_slots;
   WsLayout l;
   l.header = 0;
@@ -1376,17 +1385,18 @@ WsLayout decode_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head
 }  // namespace
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int max_ctx, int block_size, long long extra_slots) {
+                              int max_ctx, int block_size, long long extra_slots,
+                              int forced_psz) {
   return decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx, block_size,
-                       extra_slots)
+                       extra_slots, forced_psz)
       .total;
 }
 
 DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads, int num_kv_heads,
                                        int head_dim, int max_ctx, int block_size,
-                                       long long extra_slots) {
+                                       long long extra_slots, int forced_psz) {
   const WsLayout l = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_ctx,
-                                   block_size, extra_slots);
+                                   block_size, extra_slots, forced_psz);
   uint8_t* b = static_cast<uint8_t*>(ws);
   DecodeWorkspace w;
   w.header = reinterpret_cast<int*>(b + l.header);
@@ -1434,7 +1444,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(plan_threads), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
                              static_cast<int4*>(a.out), out_row_vec16, a.prefix,
-                             a.plan_wait_late ? 1 : 0);
+                             a.plan_wait_late ? 1 : 0, a.forced_part_tokens);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
   if (a.prefix.num_sharers > 0) {
     const int rc = launch_shared_prefix(a, stream);
@@ -1464,6 +1474,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // shared prefix, whose sequences' partitions start after it)
   p.prefetch_bytes = a.prefix.num_sharers > 0 ? 0 : kDecodePrefetchBytes;
   p.plan_flag = a.prefix.num_sharers > 0;
+  p.forced_psz = a.forced_part_tokens;
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {

@@ -16,7 +16,10 @@ int fail(int code, const char* fmt, ...);
 void clear_error();
 
 // Device address of the current device's status word (nullptr if unavailable).
-int32_t* status_word();
+int32_t* device_status_word();
+// The status word the kernels of a call enqueued on `stream` write: the caller's word
+// registered for that stream by pa_set_stream_status, else the device's.
+int32_t* status_word(void* stream);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
@@ -116,12 +119,16 @@ struct PrefixPlan {
   int num_sharers, prefix_len, splits, split_tokens;
 };
 
-size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size);
+// forced_psz > 0: every partition has that many tokens (the testing entry point)
+size_t decode_max_parts(int num_seqs, int num_kv_heads, int max_ctx, int block_size,
+                        int forced_psz = 0);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int max_ctx, int block_size, long long extra_slots = 0);
+                              int max_ctx, int block_size, long long extra_slots = 0,
+                              int forced_psz = 0);
 DecodeWorkspace carve_decode_workspace(void* ws, int num_seqs, int num_q_heads,
                                        int num_kv_heads, int head_dim, int max_ctx,
-                                       int block_size, long long extra_slots = 0);
+                                       int block_size, long long extra_slots = 0,
+                                       int forced_psz = 0);
 // Splits of a shared prefix: about two CTAs per SM of work, in whole 128-token tiles.
 PrefixPlan plan_prefix(int num_sharers, int prefix_len, int group, int num_kv_heads);
 
@@ -148,6 +155,9 @@ struct DecodeArgs {
   // at most this many CTAs for the attention kernel (0: one per SM), leaving the other SMs
   // to work running beside it on another stream
   int max_ctas = 0;
+  // tokens per split-KV partition, a multiple of the block size (0: chosen on the device
+  // from the batch); set only by the testing entry point
+  int forced_part_tokens = 0;
 };
 
 // Attention of a shared prefix for all of its sharers (pa_shared_prefix.cu): writes

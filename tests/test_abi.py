@@ -223,3 +223,37 @@ def test_mixed_step_rejects_bad_batches(lib, which, field, value, needle):
     setattr(dec if which == "dec" else pre, field, value)
     assert _mixed(lib, dec, pre) == 1
     assert "pa_mixed_step" in _err(lib) and needle in _err(lib)
+
+
+def test_testing_partition_workspace(lib):
+    f = lib.pa_testing_decode_workspace_bytes
+    assert f(4, 32, 8, 128, 4099, 16, 0) == 0
+    assert f(4, 32, 8, 128, 4099, 16, 129) == 0
+    sizes = [f(4, 32, 8, 128, 4099, 16, pb) for pb in (1, 2, 7, 64, 128)]
+    assert all(a >= b > 0 for a, b in zip(sizes, sizes[1:]))
+    # one block per partition: 257 partials per sequence, 32 query heads of 128 fp32 each
+    assert sizes[0] >= 4 * 257 * 32 * 128 * 4
+
+
+@pytest.mark.parametrize("pb", [0, -1, 129])
+def test_testing_partitions_rejects_sizes(lib, pb):
+    rc = lib.pa_testing_decode_partitions(FAKE, 2, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 128, 4, 32,
+                                          8, 128, 16, 64, 0.1, 2, pb, FAKE, 1 << 30, None)
+    assert rc == 1 and "part_blocks" in _err(lib)
+
+
+def test_testing_partitions_checks_workspace(lib):
+    rc = lib.pa_testing_decode_partitions(FAKE, 2, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 128, 4, 32,
+                                          8, 128, 16, 64, 0.1, 2, 1, FAKE, 1024, None)
+    assert rc == 3 and "workspace" in _err(lib)
+
+
+def test_stream_status_word_must_be_aligned(lib):
+    import torch
+    rc = lib.pa_set_stream_status(None, FAKE + 2)
+    # without a device the call cannot name one (PA_ERR_CUDA); with one, the word is checked
+    assert rc == (1 if torch.cuda.is_available() else 4)
+
+
+def test_release_with_nothing_to_release(lib):
+    assert lib.pa_release_thread_resources() == 0
