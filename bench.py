@@ -38,11 +38,15 @@ import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; KV tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
-NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context; the roofline uses the measured copy)
+# Vendor figure, context only (the roofline uses the measured copy): NVIDIA's public GB300
+# NVL72 specification gives up to 576 TB/s of HBM3e bandwidth over its 72 GPUs, 8 TB/s each.
+NOMINAL_HBM_GBS = 8000.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_53_gb300", "csrc", "pa_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 # end-to-end pass: steps shorter than this replay a captured CUDA graph (see run_ours)
 GRAPH_STEP_MS = 0.1
+# bytes written between steps of the L2-flushed passes (L2: 129 MB)
+FLUSH_BYTES = 512 << 20
 
 
 # ------------------------------------------------------------------ accounting
@@ -103,8 +107,11 @@ def prefill_algorithmic_bytes(step: W.Step, out_bytes: int) -> int:
 
 
 def measured_peaks(kind: str = "hbm"):
-    """HBM GB/s, or bf16 dense TFLOP/s (burst), from the driver's measurements."""
-    key, fallback = ("hbm_gbs", FALLBACK_HBM_GBS) if kind == "hbm" else ("bf16_tflops", 1900.0)
+    """HBM GB/s, or bf16 dense TFLOP/s (burst or sustained), from the driver's
+    measurements."""
+    key, fallback = {"hbm": ("hbm_gbs", FALLBACK_HBM_GBS),
+                     "tensor": ("bf16_tflops", 1900.0),
+                     "tensor_sustained": ("bf16_tflops_sustained", 1700.0)}[kind]
     try:
         with open(PEAKS_FILE) as f:
             p = json.load(f)
@@ -166,8 +173,9 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
@@ -175,7 +183,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -362,27 +370,74 @@ def run_ours(args, rank, world, local_rank):
     # recorded between two launches ends the programmatic-dependent-launch overlap of the
     # kernels on either side of it, which costs ~8 us per step here.  The second records
     # events around each library call, for the per-call durations of the roofline.
+    # Every pass times exactly k steps between a barrier and a synchronisation on both
+    # sides; passes repeat until --min-timed-s seconds have gone by, so that the clock
+    # sampler (one sample per 50 ms) sees the GPU under load, and the median pass is
+    # reported.  Then, in turn: passes with events around each library call (per-call
+    # durations), and passes whose steps are each preceded by a write of FLUSH_BYTES
+    # (outside the events) so that no step finds the previous one's data in L2.
     k = args.steps
     mk = lambda: torch.cuda.Event(enable_timing=True)
     evs = [(mk(), mk(), mk(), mk()) for _ in range(k)]
+    fevs = [(mk(), mk()) for _ in range(k)]
     t0, t1, t2, t3 = mk(), mk(), mk(), mk()
-    with ClockSampler(local_rank) as clocks:
-        barrier()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(FLUSH_BYTES // 8, dtype=torch.int32, device=dev)
+    pass_ms, dec_list, pre_list, evented_list, flushed_list = [], [], [], [], []
+
+    def timed_passes(body, seconds, min_passes=3):
+        t_start = time.perf_counter()
+        n = 0
+        while n < min_passes or time.perf_counter() - t_start < seconds:
+            barrier()
+            body()
+            barrier()
+            n += 1
+        return n
+
+    def plain_pass():
         t0.record(stream)
         for i in range(k):
             one_step()
         t1.record(stream)
-        step_launches = launches_per_step
-        barrier()
+        torch.cuda.synchronize(dev)
+        pass_ms.append(t0.elapsed_time(t1))
+
+    def evented_pass():
         t2.record(stream)
         for i in range(k):
             one_step(evs[i])
         t3.record(stream)
-        barrier()
-    total_ms = t0.elapsed_time(t1)
-    evented_ms = t2.elapsed_time(t3) / k
-    dec_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if d is not None else 0.0
-    pre_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs])) if p is not None else 0.0
+        torch.cuda.synchronize(dev)
+        evented_list.append(t2.elapsed_time(t3) / k)
+        if d is not None:
+            dec_list.extend(e[0].elapsed_time(e[1]) for e in evs)
+        if p is not None:
+            pre_list.extend(e[2].elapsed_time(e[3]) for e in evs)
+
+    def flushed_pass():
+        for i in range(k):
+            # the write evicts the step's data; the read then replaces the dirty lines the
+            # write left with clean ones, so that no write-back falls inside the next step
+            flush.fill_(i & 0xff)
+            flush_read.max()
+            fevs[i][0].record(stream)
+            one_step()
+            fevs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        flushed_list.extend(e[0].elapsed_time(e[1]) for e in fevs)
+
+    with ClockSampler(local_rank) as clocks:
+        n_plain = timed_passes(plain_pass, args.min_timed_s)
+        step_launches = launches_per_step
+        n_evented = timed_passes(evented_pass, args.min_timed_s / 4)
+        n_flushed = timed_passes(flushed_pass, args.min_timed_s / 4)
+    total_ms = float(np.median(pass_ms))
+    evented_ms = float(np.median(evented_list))
+    dec_ms = float(np.mean(dec_list)) if d is not None else 0.0
+    pre_ms = float(np.mean(pre_list)) if p is not None else 0.0
+    flushed_ms = float(np.mean(flushed_list))
+    del flush, flush_read
     if pa.get_status() != 0:
         raise RuntimeError("library status word set during the timed region")
 
@@ -494,19 +549,26 @@ def run_ours(args, rank, world, local_rank):
                ("replayed from a CUDA graph" if graphs else "issued from the host"))
 
     step_ms = total_ms / k
-    step_ms, dec_ms, pre_ms, e2e_ms, evented_ms = slowest_over_ranks(
-        [step_ms, dec_ms, pre_ms, e2e_ms, evented_ms], world, device=dev)
+    step_ms, dec_ms, pre_ms, e2e_ms, evented_ms, flushed_ms = slowest_over_ranks(
+        [step_ms, dec_ms, pre_ms, e2e_ms, evented_ms, flushed_ms], world, device=dev)
 
     config = {
         "workload": step.name, "num_q_heads": sh.num_q_heads, "num_kv_heads": sh.num_kv_heads,
         "head_dim": sh.head_dim, "block_size": sh.block_size,
         "cow_copies": int(step.cow_pairs.shape[0]) if step.cow_pairs is not None else 0,
         "parallelism": f"replicas x{world}",
-        "timing": ("step: k steps with no event between kernels; per-call durations: a "
-                   f"second pass of k steps with events around each call ({evented_ms:.5f} "
-                   "ms per step in that pass)"
+        "timing": (f"step: median of {n_plain} passes of exactly k steps (repeated for at "
+                   f"least {args.min_timed_s:g} s), no event between kernels; per-call "
+                   f"durations: {n_evented} passes of k steps with events around each call "
+                   f"({evented_ms:.5f} ms per step there); L2-flushed: {n_flushed} passes whose "
+                   f"steps each follow a {FLUSH_BYTES >> 20} MiB write and a "
+                   f"{FLUSH_BYTES >> 21} MiB read outside the events"
                    + ("; the step is one pa_mixed_step call (decode and prefill side by side), "
                       "the per-call pass runs them as separate calls" if mixed else "")),
+        "l2_flush": (f"value: inputs larger than L2, no flush between steps; "
+                     f"value_l2_flushed: a {FLUSH_BYTES >> 20} MiB write then a "
+                     f"{FLUSH_BYTES >> 21} MiB read before every step (events around each step, "
+                     "compare with value_evented, which has the events but no flush)"),
     }
     if share:
         config["shared_prefix"] = {"sharers": int(len(sharers)), "prefix_len": int(plen),
@@ -547,6 +609,8 @@ def run_ours(args, rank, world, local_rank):
                       "vs 0.13 GB L2"})
         res.update({
             "value": round(world * kvb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "value_l2_flushed": round(world * kvb / (flushed_ms * 1e-3) / 1e9, 1),
+            "value_evented": round(world * kvb / (evented_ms * 1e-3) / 1e9, 1),
             "kv_tokens_per_s": round(world * kv_tokens / (step_ms * 1e-3), 1),
             "hbm_frac_of_measured": round(kvb / (step_ms * 1e-3) / 1e9 / peak, 4),
             "hbm_frac_of_nominal": round(kvb / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
@@ -584,6 +648,7 @@ def run_ours(args, rank, world, local_rank):
         res.update({
             "metric": "chunked-prefill attention useful TFLOP/s",
             "value": round(world * flops / (step_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "value_l2_flushed": round(world * flops / (flushed_ms * 1e-3) / 1e12, 1),
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5), "steps": ke,
@@ -594,6 +659,145 @@ def run_ours(args, rank, world, local_rank):
     res["clocks"] = clocks.summary()
     res["gpu_launches"] = step_launches * k
     return res, step
+
+
+# ------------------------------------------------------------------ secondary calls
+def _device_inputs(step: W.Step, dev):
+    import torch
+    vals = W.make_values(step, dev)
+    meta = {}
+    for kind in ("decode", "prefill"):
+        b = getattr(step, kind)
+        if b is None:
+            continue
+        meta[kind] = {"bt": torch.from_numpy(b.block_tables).to(dev),
+                      "ctx": torch.from_numpy(b.context_lens).to(dev),
+                      "cu": torch.from_numpy(b.cu_q_lens).to(dev)}
+    return vals, meta
+
+
+def _time_call(call, seconds: float, stream, dev, per_pass: int = 20, warmup: int = 5):
+    """Mean device time of `call` (ms): passes of `per_pass` back-to-back calls with an
+    event pair around each, repeated until `seconds` have passed; clocks sampled meanwhile."""
+    import torch
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    evs = [(mk(), mk()) for _ in range(per_pass)]
+    times = []
+    with ClockSampler(dev.index or 0) as clocks:
+        t_start = time.perf_counter()
+        while not times or time.perf_counter() - t_start < seconds:
+            for a, b in evs:
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.extend(a.elapsed_time(b) for a, b in evs)
+    return float(np.mean(times)), len(times), clocks.summary()
+
+
+def run_extras(args, dev):
+    """The hot path's other calls on their own workloads, each timed alone after the
+    headline (pools built one at a time and freed in turn): the chunked prefill of the
+    mixed workload against the tensor roofline, the prefix-sharing decode against HBM on
+    its unique bytes, and the OPT-13B-shaped decode step against HBM."""
+    import torch
+    import paged_kv_cache_53_gb300 as pa
+    stream = torch.cuda.current_stream(dev)
+    hbm, hbm_kind = measured_peaks()
+    tpeak, tkind = measured_peaks("tensor")
+    tsus = measured_peaks("tensor_sustained")[0]
+    out = {}
+    seconds = args.extra_timed_s
+
+    # chunked prefill: 8 chunks of 512 tokens over 0..16,384 tokens of paged context
+    step = W.mixed_prefill_only()
+    sh, p = step.shape, step.prefill
+    vals, meta = _device_inputs(step, dev)
+    kc, vc, m = vals["k_cache"], vals["v_cache"], meta["prefill"]
+    pa.cache_append(vals["k_new_prefill"], vals["v_new_prefill"], kc, vc, m["bt"], m["cu"],
+                    m["ctx"], p.max_q)
+    o = torch.empty((p.num_new_tokens, sh.num_q_heads, sh.head_dim), dtype=kc.dtype, device=dev)
+    ws = torch.empty(max(16, pa.prefill_workspace_bytes(p.num_seqs, p.num_new_tokens, p.max_q,
+                                                        sh.num_q_heads, sh.num_kv_heads,
+                                                        sh.head_dim, p.max_ctx, sh.block_size)),
+                     dtype=torch.uint8, device=dev)
+    ms, n, clk = _time_call(lambda: pa.prefill_chunk(o, vals["q_prefill"], kc, vc, m["bt"],
+                                                     m["cu"], m["ctx"], p.max_q, p.max_ctx,
+                                                     step.scale, ws), seconds, stream, dev)
+    flops = prefill_useful_flops(step)
+    tf = flops / (ms * 1e-3) / 1e12
+    out["prefill_call"] = {
+        "workload": step.name, "call": "pa_prefill_chunk", "ms_per_call": round(ms, 5),
+        "calls_timed": n, "clocks": clk,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak,
+                     "peak_kind": f"{tkind} bf16 dense, burst", "unit": "TFLOP/s",
+                     "frac": round(tf / tpeak, 4), "frac_of_sustained": round(tf / tsus, 4),
+                     "useful_gflop": round(flops / 1e9, 2), "traffic": None}}
+    del vals, meta, kc, vc, m, o, ws
+    torch.cuda.empty_cache()
+
+    # prefix sharing: 128 sequences on one 2,048-token prefix + 8 groups of 4 samples
+    step = W.prefix_sharing_cow()
+    sh, d = step.shape, step.decode
+    vals, meta = _device_inputs(step, dev)
+    kc, vc, m = vals["k_cache"], vals["v_cache"], meta["decode"]
+    pa.copy_blocks([kc], [vc], torch.from_numpy(step.cow_pairs).to(dev))
+    pa.cache_append(vals["k_new_decode"], vals["v_new_decode"], kc, vc, m["bt"], m["cu"],
+                    m["ctx"], 1)
+    pblocks, plen, sharers = step.shared_prefix
+    pb_t, sh_t = torch.from_numpy(pblocks).to(dev), torch.from_numpy(sharers).to(dev)
+    o = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=kc.dtype, device=dev)
+    ws = torch.empty(pa.decode_shared_prefix_workspace_bytes(
+        d.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, d.max_ctx, sh.block_size,
+        len(sharers), plen), dtype=torch.uint8, device=dev)
+    ms, n, clk = _time_call(lambda: pa.decode_shared_prefix(o, vals["q_decode"], kc, vc, m["bt"],
+                                                            m["ctx"], d.max_ctx, pb_t, plen,
+                                                            sh_t, step.scale, ws),
+                            seconds, stream, dev)
+    alg = decode_algorithmic_bytes(step, o.element_size(), shared=True)
+    gbs = alg / (ms * 1e-3) / 1e9
+    out["shared_prefix_call"] = {
+        "workload": step.name, "call": "pa_decode_shared_prefix", "ms_per_call": round(ms, 5),
+        "calls_timed": n, "clocks": clk,
+        "logical_kv_gbs": round(kv_bytes(step) / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                     "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "algorithmic_bytes": alg, "traffic": None,
+                     "how": "unique bytes: the shared prefix's K/V and block entries once"}}
+    del vals, meta, kc, vc, m, o, ws, pb_t, sh_t
+    torch.cuda.empty_cache()
+
+    # OPT-13B-shaped decode step (MHA, 40 heads, fp16): cache write + decode in one call
+    step = W.opt13b_decode()
+    sh, d = step.shape, step.decode
+    vals, meta = _device_inputs(step, dev)
+    kc, vc, m = vals["k_cache"], vals["v_cache"], meta["decode"]
+    o = torch.empty((d.num_seqs, sh.num_q_heads, sh.head_dim), dtype=kc.dtype, device=dev)
+    ws = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads, sh.num_kv_heads,
+                                               sh.head_dim, d.max_ctx, sh.block_size),
+                     dtype=torch.uint8, device=dev)
+    ms, n, clk = _time_call(lambda: pa.decode_append(o, vals["q_decode"], vals["k_new_decode"],
+                                                     vals["v_new_decode"], kc, vc, m["bt"],
+                                                     m["ctx"], d.max_ctx, step.scale, ws),
+                            seconds, stream, dev)
+    alg = decode_algorithmic_bytes(step, o.element_size())
+    alg += 2 * 2 * d.num_seqs * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+    gbs = alg / (ms * 1e-3) / 1e9
+    out["opt13b_decode_call"] = {
+        "workload": step.name, "call": "pa_decode_append", "ms_per_call": round(ms, 5),
+        "calls_timed": n, "clocks": clk,
+        "kv_gbs": round(kv_bytes(step) / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                     "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "algorithmic_bytes": alg, "traffic": None}}
+    del vals, meta, kc, vc, m, o, ws
+    torch.cuda.empty_cache()
+    if pa.get_status() != 0:
+        raise RuntimeError("library status word set while timing the secondary calls")
+    return out
 
 
 # ------------------------------------------------------------------ swap (pre-emption)
@@ -742,10 +946,6 @@ def _oracle_worker(payload):
     return time.perf_counter() - t, int(ctx.astype(np.int64).sum())
 
 
-def _payload_tokens(payload) -> int:
-    return int(payload[4].astype(np.int64).sum())
-
-
 def _oracle_payload(step: W.Step, seqs, gen):
     """The listed sequences of the workload with a pool of just their blocks (random
     values, same shapes and lengths), tables renumbered into that pool."""
@@ -819,16 +1019,6 @@ class OraclePool:
         self.pool.map(_oracle_worker, payloads, chunksize=1)
         return time.perf_counter() - t
 
-    @staticmethod
-    def time_single(payloads):
-        """Wall time of the payloads run one after another by a single spawned
-        single-threaded worker."""
-        pool = OraclePool(1)
-        try:
-            return pool.time(payloads)
-        finally:
-            pool.close()
-
     def close(self):
         self.pool.close()
         self.pool.join()
@@ -843,6 +1033,33 @@ def host_cores():
     return min(len(os.sched_getaffinity(0)), 16)
 
 
+def _oracle_full_pass(name: str):
+    """Run in a spawned single-threaded worker: the whole decode batch of workload `name`
+    (every sequence, random values of the same shapes and lengths) through the oracle.
+    Returns (seconds of oracle work, KV bytes read); generating the inputs is not timed."""
+    import torch
+    step = W.NAMED[name]()
+    gen = torch.Generator().manual_seed(step.seed)
+    payload = _oracle_payload(step, list(range(step.decode.num_seqs)), gen)
+    secs, toks = _oracle_worker(payload)
+    sh = step.shape
+    return secs, toks * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+
+
+def single_thread_oracle(names=("opt13b_decode", "llama8b_gqa_decode")):
+    """One full single-threaded oracle pass over each named decode workload."""
+    pool = OraclePool(1)
+    res = {}
+    try:
+        for name in names:
+            secs, nbytes = pool.pool.apply(_oracle_full_pass, (name,))
+            res[name] = {"seconds": round(secs, 3), "value": round(nbytes / secs / 1e9, 4),
+                         "unit": "GB/s", "kv_bytes": int(nbytes)}
+    finally:
+        pool.close()
+    return res
+
+
 def cpu_baseline(step: W.Step, budget_s: float):
     cores = host_cores()
     payloads, desc, kvb = make_oracle_sample(step, budget_s, cores)
@@ -850,17 +1067,15 @@ def cpu_baseline(step: W.Step, budget_s: float):
     pool = OraclePool(workers)
     try:
         wall = pool.time(payloads)
-        # one worker alone on a slice of the same sample (about the same per-core budget)
-        one = payloads[:1]
-        one_bytes = sum(_payload_tokens(q) for q in one) * 2 * step.shape.num_kv_heads * \
-            step.shape.head_dim * step.shape.elem_bytes
-        t1 = OraclePool.time_single(one)
     finally:
         pool.close()
+    single = single_thread_oracle()
+    single["how"] = ("one full pass of each workload's whole decode batch by one spawned "
+                     "single-threaded worker, wall seconds of the oracle's work (input "
+                     "generation excluded)")
     return {"value": round(kvb / wall / 1e9, 4), "unit": "GB/s", "cores": workers,
             "kind": "oracle", "sample": desc, "seconds": round(wall, 2),
-            "single_thread": {"value": round(one_bytes / t1 / 1e9, 4), "unit": "GB/s",
-                              "seconds": round(t1, 2), "sample": "one worker's share"}}
+            "single_thread": single}
 
 
 def run_reference(args, world):
@@ -910,6 +1125,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.NAMED), default="llama8b_gqa_decode")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="the k-step timed pass repeats until this many seconds have passed")
+    ap.add_argument("--extra-timed-s", type=float, default=0.5,
+                    help="seconds of timed calls for each secondary call")
+    ap.add_argument("--extras", choices=["on", "off"], default="on",
+                    help="on: after the headline, time the prefill, shared-prefix and "
+                         "OPT-13B-shaped decode calls on their own workloads")
     ap.add_argument("--mixed-step", choices=["on", "off"], default="on",
                     help="on: a batch of decodes and prefill chunks in one pa_mixed_step call "
                          "(the two side by side on disjoint SMs); off: the calls in turn")
@@ -971,6 +1193,9 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res, step = run_ours(args, rank, world, local_rank)
+    if args.extras == "on" and world == 1 and args.workload == "llama8b_gqa_decode":
+        import torch
+        res.update(run_extras(args, torch.device("cuda", local_rank)))
     if rank == 0 and not args.no_cpu_baseline and world == 1 and step.decode is not None:
         res["cpu_baseline"] = cpu_baseline(step, args.cpu_budget_s)
     if world > 1:
