@@ -62,34 +62,48 @@ struct PrefillParams {
   float scale_log2;
 };
 
-template <int D, int BS>
+template <int D, int BS, bool PAIR>
 struct PrefillCfg {
-  static constexpr int BM = 128;                       // query rows per tile
+  // PAIR: a cluster of two CTAs on two SMs shares every product (tcgen05 cta_group::2,
+  // M = 256): each CTA holds 128 of the 256 query rows, half of each K tile (64 of its
+  // 128 tokens) and half of each V tile (64 of its 128 columns), so that the operand
+  // bytes each SM reads from its own shared memory per product, the K/V bytes its TMA
+  // writes and the V bytes it converts are all smaller than with one CTA per product.
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int BM = 128;                       // query rows per tile, per CTA
   static constexpr int kTiles = 2;                     // query tiles per CTA (ping-pong)
   static constexpr int BN = 128;                       // context tokens per K/V tile
-  static constexpr int kHalves = D / 64;               // 128-byte column groups
+  static constexpr int kHalves = D / 64;               // 128-byte column groups of a row
   static constexpr int kQHalfBytes = BM * 128;         // 16 KiB
   static constexpr int kQBytes = kHalves * kQHalfBytes;
-  static constexpr int kKvHalfBytes = BN * 128;        // 16 KiB
-  static constexpr int kKBytes = kHalves * kKvHalfBytes;
+  static constexpr int kKRows = BN / kCtas;            // K tile rows (tokens) per CTA
+  static constexpr int kKHalfBytes = kKRows * 128;
+  static constexpr int kKBytes = kHalves * kKHalfBytes;
+  static constexpr int kVHalves = kHalves / kCtas;     // V tile column groups per CTA
+  static constexpr int kVHalfBytes = BN * 128;
+  static constexpr int kVBytes = kVHalves * kVHalfBytes;
   // separate rings for K and V tiles.  V(j+1) is converted as soon as P(j) is out, and
-  // its slot frees only when both P(j-1) V(j-1) products are done: with two V stages its
-  // load would start about one step before it is needed, less than a load's latency, and
-  // the softmax warpgroups would wait for it.  A third V stage starts the load a step
-  // earlier.
-  static constexpr int kKStages = D == 128 ? 2 : 4;
+  // its slot frees only when both P(j-1) V(j-1) products are done: with as many V stages
+  // as K stages its load would start about one step before it is needed, less than a
+  // load's latency, and the softmax warpgroups would wait for it.  One more V stage starts
+  // the load a step earlier.
+  static constexpr int kKStages = PAIR ? 3 : (D == 128 ? 2 : 4);
   static constexpr int kVStages = kKStages + 1;
   static constexpr int kBlocksPerTile = BN / BS;
+  static constexpr int kKBlocks = kKRows / BS;         // K blocks each CTA loads per tile
   static constexpr int kThreads = 384;                 // producer, MMA, 2 converters, 2 softmax WGs
   static constexpr int kVThreads = 256;                // threads converting V
   static constexpr int kTmemCols = 512;                // S/P_A | S/P_B | O_A | O_B
+  // arrivals on the first CTA's v_ready / p_full: one per converting warp / softmax warp
+  // of each CTA
+  static constexpr int kVReadyArrivals = kVThreads / 32 * kCtas;
+  static constexpr int kPFullArrivals = 4 * kCtas;
   // barriers: q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], v_ready[SV], then
   // per query tile s_full, p_full, pv_done.  K(j) is done with once S(j) has been
   // computed, an iteration before P(j) V(j), so the next K tile loads that much earlier.
   static constexpr int kBars = 1 + 2 * kKStages + 3 * kVStages + 3 * kTiles;
-  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes +
-                                  (size_t)(kKStages + kVStages) * kKBytes +
-                                  kBars * 8 + 16;
+  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + kKStages * (size_t)kKBytes +
+                                  kVStages * (size_t)kVBytes + kBars * 8 + 16;
 };
 
 template <typename T>
@@ -200,27 +214,27 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
 }
 
-// Per query tile of a CTA: where it starts in the chunk and how far it reaches.
+// Per query tile: where it starts in the chunk and how far it reaches.
 struct TileGeom {
   int t0;       // first chunk token
   int ntok;     // chunk tokens in the tile (0: the tile lies past the chunk)
   int n_kv;     // K/V tiles it needs (0 if ntok == 0)
 };
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool PAIR>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-  using C = PrefillCfg<D, BS>;
-  constexpr int BN = C::BN, SK = C::kKStages, SV = C::kVStages, NT = C::kTiles;
+  using C = PrefillCfg<D, BS, PAIR>;
+  constexpr int BN = C::BN, SK = C::kKStages, SV = C::kVStages, NT = C::kTiles, NC = C::kCtas;
   static_assert(C::kSmem <= 232448, "shared memory per CTA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = base;                              // [tile][half][128 rows][128 B]
-  uint8_t* sK = sQ + NT * C::kQBytes;              // [K stage][half][128 rows][128 B]
+  uint8_t* sK = sQ + NT * C::kQBytes;              // [K stage][half][kKRows rows][128 B]
   uint8_t* sV = sK + SK * C::kKBytes;              // [V stage][half][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kKBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kVBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -234,31 +248,55 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int tpt = C::BM / G;  // chunk tokens per query tile
+  const int tpt = C::BM / G;  // chunk tokens per query tile of one CTA
+  // rank 0 of a pair issues the MMAs; q_full, k_full, p_full and v_ready of rank 0 count
+  // both CTAs' copies and arrivals, the other barriers are each CTA's own
+  const int crank = PAIR ? (int)cluster_ctarank() : 0;
+  const bool leader = crank == 0;
+  // waits on barriers the peer CTA may complete take cluster-scope acquire
+  auto wait = [](uint64_t* bar, uint32_t parity) {
+    return PAIR ? mbar_wait_cluster(smem_addr(bar), parity) : mbar_wait(smem_addr(bar), parity);
+  };
+  // the address of rank 0's copy of a barrier, for copies and arrivals aimed at it
+  auto lead = [](uint64_t* bar) {
+    return PAIR ? mapa_shared(smem_addr(bar), 0) : smem_addr(bar);
+  };
+  // an arrival on rank 0's copy of a barrier
+  auto arrive_lead = [&](uint64_t* bar) {
+    if (PAIR && !leader) mbar_arrive_remote(lead(bar));
+    else mbar_arrive(smem_addr(bar));
+  };
 
   griddep_wait();  // the work list and the chunk's K/V (cache write) are complete
-  if ((int)blockIdx.x >= __ldg(p.header)) return;  // more CTAs launched than items
-  const PrefillItem item = p.items[blockIdx.x];
+  // every exit before the barriers are set up is taken by both CTAs of a pair together
+  const int it = (int)blockIdx.x / NC;
+  if (it >= __ldg(p.header)) return;  // more CTAs launched than items
+  const PrefillItem item = p.items[it];
   const int h = item.h, b = item.b;
   const int q_begin = __ldg(p.cu_q_lens + b);
   const int chunk = __ldg(p.cu_q_lens + b + 1) - q_begin;
-  const int t0_cta = item.ctile * NT * tpt;
-  if (t0_cta >= chunk) return;  // the whole CTA leaves before touching any barrier
+  const int t0_item = item.ctile * NT * NC * tpt;
+  if (t0_item >= chunk) return;
   const int ctx = __ldg(p.context_lens + b);
   if (ctx < chunk || (long long)ctx > (long long)p.max_blocks * BS) {
-    if (threadIdx.x == 0 && item.ctile == 0 && h == 0) flag_status(p.status, PA_STATUS_BAD_CONTEXT);
+    if (threadIdx.x == 0 && leader && item.ctile == 0 && h == 0)
+      flag_status(p.status, PA_STATUS_BAD_CONTEXT);
     return;
   }
   const int ctx0 = ctx - chunk;
   const int nblk_ctx = (ctx + BS - 1) / BS;
-  TileGeom tg[NT];
+  // pg: the product's query tile x (both CTAs' rows), tg: this CTA's rows of it
+  TileGeom pg[NT], tg[NT];
 #pragma unroll
   for (int x = 0; x < NT; ++x) {
-    tg[x].t0 = t0_cta + x * tpt;
+    pg[x].t0 = t0_item + x * NC * tpt;
+    pg[x].ntok = max(0, min(NC * tpt, chunk - pg[x].t0));
+    pg[x].n_kv = pg[x].ntok > 0 ? (ctx0 + pg[x].t0 + pg[x].ntok - 1) / BN + 1 : 0;
+    tg[x].t0 = pg[x].t0 + crank * tpt;
     tg[x].ntok = max(0, min(tpt, chunk - tg[x].t0));
-    tg[x].n_kv = tg[x].ntok > 0 ? (ctx0 + tg[x].t0 + tg[x].ntok - 1) / BN + 1 : 0;
+    tg[x].n_kv = pg[x].n_kv;
   }
-  const int n_kv = tg[NT - 1].ntok > 0 ? tg[NT - 1].n_kv : tg[0].n_kv;  // the CTA's K/V tiles
+  const int n_kv = pg[NT - 1].ntok > 0 ? pg[NT - 1].n_kv : pg[0].n_kv;  // the item's K/V tiles
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(q_full), 1);
@@ -269,18 +307,23 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < SV; ++i) {
       mbar_init(smem_addr(v_full + i), 1);
       mbar_init(smem_addr(v_empty + i), 1);
-      mbar_init(smem_addr(v_ready + i), C::kVThreads);
+      mbar_init(smem_addr(v_ready + i), C::kVReadyArrivals);
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(smem_addr(s_full + x), 1);
-      mbar_init(smem_addr(p_full + x), 128);
+      mbar_init(smem_addr(p_full + x), C::kPFullArrivals);
       mbar_init(smem_addr(pv_done + x), 1);
     }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(smem_addr(tmem_slot), C::kTmemCols);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   if (threadIdx.x == 32 + 1) {
     prefetch_tensormap(&tmq);
@@ -288,7 +331,8 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tensormap(&tmv);
   }
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either uses them
+  else __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // TMEM columns: S of tile x at x * BN (P_x is written over its first half: token t of
@@ -305,12 +349,13 @@ __global__ void __launch_bounds__(384, 1)
     vt = 64 + 32 * (q - (q >= 2 ? 1 : 0) - (q >= 6 ? 1 : 0)) + lane;
   }
   __half2 vmax = __floats2half2_rn(0.f, 0.f);  // largest |v| converted, per lane half
+  // called by whole warps
   auto convert_v = [&](int jv) -> bool {
     const int s = jv % SV;
-    if (!mbar_wait(smem_addr(v_full + s), (jv / SV) & 1)) return false;
+    if (!__all_sync(~0u, mbar_wait(smem_addr(v_full + s), (jv / SV) & 1))) return false;
     const int z0 = ctx - jv * BN;  // rows from z0 on lie past the context
-    uint4* sv = reinterpret_cast<uint4*>(sV + s * C::kKBytes);
-    constexpr int kPer = C::kKBytes / 16 / C::kVThreads;
+    uint4* sv = reinterpret_cast<uint4*>(sV + s * C::kVBytes);
+    constexpr int kPer = C::kVBytes / 16 / C::kVThreads;
     uint4 v[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) v[u] = sv[vt + u * C::kVThreads];
@@ -319,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
       // a piece's row: rows are 128 bytes in every 64-column half (the swizzle only
       // permutes pieces within a row); pieces past the context become zeros
       const int i = vt + u * C::kVThreads;
-      if (z0 < BN && ((i % (C::kKvHalfBytes / 16)) >> 3) >= z0) {
+      if (z0 < BN && ((i % (C::kVHalfBytes / 16)) >> 3) >= z0) {
         v[u] = make_uint4(0, 0, 0, 0);
       } else if constexpr (Fmt<T>::v == 1) {
         uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
@@ -335,7 +380,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
     for (int u = 0; u < kPer; ++u) sv[vt + u * C::kVThreads] = v[u];
     tc::fence_proxy_async_smem();  // the tensor core reads what the threads wrote
-    mbar_arrive(smem_addr(v_ready + s));
+    __syncwarp();
+    if (lane == 0) arrive_lead(v_ready + s);
     return true;
   };
 
@@ -345,15 +391,19 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       int qbytes = 0;
 #pragma unroll
-      for (int x = 0; x < NT; ++x) qbytes += tg[x].ntok > 0 ? C::kQBytes : 0;
-      mbar_arrive_expect_tx(smem_addr(q_full), qbytes);
+      for (int x = 0; x < NT; ++x) qbytes += pg[x].ntok > 0 ? C::kQBytes : 0;
+      if (leader) mbar_arrive_expect_tx(smem_addr(q_full), qbytes * NC);
 #pragma unroll
       for (int x = 0; x < NT; ++x) {
-        if (tg[x].ntok == 0) continue;
+        if (pg[x].ntok == 0) continue;
 #pragma unroll
-        for (int hb = 0; hb < C::kHalves; ++hb)
-          tma_load_3d(smem_addr(sQ + x * C::kQBytes + hb * C::kQHalfBytes), &tmq, hb * 64, h * G,
-                      q_begin + tg[x].t0, smem_addr(q_full), keep);
+        for (int hb = 0; hb < C::kHalves; ++hb) {
+          const uint32_t dst = smem_addr(sQ + x * C::kQBytes + hb * C::kQHalfBytes);
+          if constexpr (PAIR)
+            tma_load_3d_pair(dst, &tmq, hb * 64, h * G, q_begin + tg[x].t0, lead(q_full), keep);
+          else
+            tma_load_3d(dst, &tmq, hb * 64, h * G, q_begin + tg[x].t0, smem_addr(q_full), keep);
+        }
       }
     }
     const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
@@ -367,27 +417,37 @@ __global__ void __launch_bounds__(384, 1)
           id = -1;
         }
       }
-      // K of tile j, then its V, each once its slot's previous tile is done with
+      // K of tile j (this CTA's rows of it), once its slot's previous tile is done with
+      const int sk = j % SK;
+      if (!__all_sync(~0u, wait(k_empty + sk, ((j / SK) & 1) ^ 1))) { ok = false; break; }
+      if (lane == 0 && leader) mbar_arrive_expect_tx(smem_addr(k_full + sk), C::kKBytes * NC);
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const int ns = kv == 0 ? SK : SV, s = j % ns;
-        uint64_t* full = kv == 0 ? k_full : v_full;
-        uint64_t* empty = kv == 0 ? k_empty : v_empty;
-        if (!mbar_wait(smem_addr(empty + s), ((j / ns) & 1) ^ 1)) { ok = false; break; }
-        uint8_t* st = (kv == 0 ? sK : sV) + s * C::kKBytes;
-        const CUtensorMap* map = kv == 0 ? &tmk : &tmv;
-        if (lane == 0) mbar_arrive_expect_tx(smem_addr(full + s), C::kKBytes);
+      for (int i = 0; i < C::kKBlocks; ++i) {
+        const int idi = __shfl_sync(~0u, id, crank * C::kKBlocks + i);
+        if (lane == 0) {
+          // blocks past the context (and bad ids) read a box wholly outside: zeros
+          const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
 #pragma unroll
-        for (int i = 0; i < C::kBlocksPerTile; ++i) {
-          const int idi = __shfl_sync(~0u, id, i);
-          if (lane == 0) {
-            // blocks past the context (and bad ids) read a box wholly outside: zeros
-            const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
-#pragma unroll
-            for (int hb = 0; hb < C::kHalves; ++hb)
-              tma_load_2d(smem_addr(st + hb * C::kKvHalfBytes + i * BS * 128), map, hb * 64, y,
-                          smem_addr(full + s), keep);
+          for (int hb = 0; hb < C::kHalves; ++hb) {
+            const uint32_t dst = smem_addr(sK + sk * C::kKBytes + hb * C::kKHalfBytes + i * BS * 128);
+            if constexpr (PAIR) tma_load_2d_pair(dst, &tmk, hb * 64, y, lead(k_full + sk), keep);
+            else tma_load_2d(dst, &tmk, hb * 64, y, smem_addr(k_full + sk), keep);
           }
+        }
+      }
+      // V of tile j (this CTA's columns of it) into its own stage
+      const int sv = j % SV;
+      if (!__all_sync(~0u, wait(v_empty + sv, ((j / SV) & 1) ^ 1))) { ok = false; break; }
+      if (lane == 0) mbar_arrive_expect_tx(smem_addr(v_full + sv), C::kVBytes);
+#pragma unroll
+      for (int i = 0; i < C::kBlocksPerTile; ++i) {
+        const int idi = __shfl_sync(~0u, id, i);
+        if (lane == 0) {
+          const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
+#pragma unroll
+          for (int hv = 0; hv < C::kVHalves; ++hv)
+            tma_load_2d(smem_addr(sV + sv * C::kVBytes + hv * C::kVHalfBytes + i * BS * 128), &tmv,
+                        (crank * C::kVHalves + hv) * 64, y, smem_addr(v_full + sv), keep);
         }
       }
     }
@@ -397,69 +457,84 @@ __global__ void __launch_bounds__(384, 1)
     // Order: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ...  While one tile's softmax runs,
     // the tensor core works through the other tile's P.V and next S.  S_x(j+1) reuses
     // the TMEM columns PV_x(j) reads P from; tcgen05.mma operations issued by one thread
-    // execute in order, so no wait is needed between the two.
-    if (lane == 0) {
-      const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM, BN, false, false);
-      const uint32_t id_o = tc::idesc_f16(Fmt<__half>::v, C::BM, D, false, true);  // fp16 P, V
-      // descriptors of each operand's first k-step, advanced by constant offsets below
-      uint64_t dq[NT];
-#pragma unroll
-      for (int x = 0; x < NT; ++x) dq[x] = tc::smem_desc_sw128(smem_addr(sQ + x * C::kQBytes), 16, 1024);
-      auto issue_s = [&](int x, int j) {
+    // execute in order, so no wait is needed between the two.  In a pair only rank 0
+    // issues; its commits arrive on the barrier of both CTAs.
+    if (leader) {
+      // the whole warp runs the loop (waits included, so that it never diverges); one
+      // elected lane issues each MMA and commit
+      auto wait_w = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(~0u, wait(bar, parity));
+      };
+      const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM * NC, BN, false, false);
+      const uint32_t id_o = tc::idesc_f16(Fmt<__half>::v, C::BM * NC, D, false, true);  // fp16 P, V
+      auto commit = [](uint64_t* bar) { tc::commit_warp<PAIR>(smem_addr(bar)); };
+      // descriptors of each operand's first k-step and first stage, advanced by constant
+      // offsets below
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(sK), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sV), C::kVHalfBytes, 1024);
+      auto issue_s = [&](int x, int sk) {
         const uint32_t tS = tmem + x * BN;
-        const uint64_t dk = tc::smem_desc_sw128(smem_addr(sK + (j % SK) * C::kKBytes), 16, 1024);
+        const uint64_t dq = tc::desc_advance(dq0, x * C::kQBytes);
+        const uint64_t dk = tc::desc_advance(dk0, sk * C::kKBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          tc::mma_f16_ss(tS, tc::desc_advance(dq[x], (kk >> 2) * C::kQHalfBytes + koff),
-                         tc::desc_advance(dk, (kk >> 2) * C::kKvHalfBytes + koff), id_s, kk > 0);
+          tc::mma_ss_warp<PAIR>(tS, tc::desc_advance(dq, (kk >> 2) * C::kQHalfBytes + koff),
+                                tc::desc_advance(dk, (kk >> 2) * C::kKHalfBytes + koff), id_s,
+                                kk > 0);
         }
-        tc::commit(smem_addr(s_full + x));
+        commit(s_full + x);
       };
       int v_seen = -1;  // last K/V tile whose fp16 V was waited for
-      auto issue_pv = [&](int x, int j) -> bool {
-        if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
+      auto issue_pv = [&](int x, int j, int sv, uint32_t vpar) -> bool {
+        if (!wait_w(p_full + x, j & 1)) return false;
         if (v_seen < j) {
-          if (!mbar_wait(smem_addr(v_ready + j % SV), (j / SV) & 1)) return false;
+          if (!wait_w(v_ready + sv, vpar)) return false;
           v_seen = j;
         }
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint64_t dv =
-            tc::smem_desc_sw128(smem_addr(sV + (j % SV) * C::kKBytes), C::kKvHalfBytes, 1024);
+        const uint64_t dv = tc::desc_advance(dv0, sv * C::kVBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          tc::mma_f16_ts(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o, j > 0 || ks > 0);
-        tc::commit(smem_addr(pv_done + x));
+          tc::mma_ts_warp<PAIR>(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o,
+                                j > 0 || ks > 0);
+        commit(pv_done + x);
         return true;
       };
-      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(k_full), 0)) ok = false;
+      if (!wait_w(q_full, 0) || !wait_w(k_full, 0)) ok = false;
       if (ok) {
         tc::fence_after_sync();
 #pragma unroll
         for (int x = 0; x < NT; ++x)
-          if (tg[x].n_kv > 0) issue_s(x, 0);
-        tc::commit(smem_addr(k_empty));  // K(0) is read once both S(0) are done
+          if (pg[x].n_kv > 0) issue_s(x, 0);
+        commit(k_empty);  // K(0) is read once both S(0) are done
       }
+      // stages and phase parities of step j's V and step j+1's K, advanced without divisions
+      int sv = 0, sk1 = SK > 1 ? 1 : 0;
+      uint32_t vpar = 0, kpar1 = SK > 1 ? 0 : 1;
       for (int j = 0; j < n_kv && ok; ++j) {
         bool next_ready = false;
 #pragma unroll
         for (int x = 0; x < NT; ++x) {
-          if (j < tg[x].n_kv && !issue_pv(x, j)) { ok = false; break; }
-          if (j + 1 < tg[x].n_kv) {
+          if (j < pg[x].n_kv && !issue_pv(x, j, sv, vpar)) { ok = false; break; }
+          if (j + 1 < pg[x].n_kv) {
             if (!next_ready) {
-              if (!mbar_wait(smem_addr(k_full + (j + 1) % SK), ((j + 1) / SK) & 1)) { ok = false; break; }
+              if (!wait_w(k_full + sk1, kpar1)) { ok = false; break; }
               tc::fence_after_sync();
               next_ready = true;
             }
-            issue_s(x, j + 1);
+            issue_s(x, sk1);
           }
         }
-        tc::commit(smem_addr(v_empty + j % SV));                    // V(j): both PV(j) issued
-        if (j + 1 < n_kv) tc::commit(smem_addr(k_empty + (j + 1) % SK));  // K(j+1): both S
+        commit(v_empty + sv);                          // V(j): both PV(j) issued
+        if (j + 1 < n_kv) commit(k_empty + sk1);       // K(j+1): both S
+        if (++sv == SV) { sv = 0; vpar ^= 1; }
+        if (++sk1 == SK) { sk1 = 0; kpar1 ^= 1; }
       }
-      if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
+      if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 2 || warp == 3) {
@@ -477,7 +552,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_bits + x * BN;
     const uint32_t tO = tmem + lane_bits + NT * BN + x * D;
-    const TileGeom g = x == 0 ? tg[0] : tg[NT - 1];
+    const TileGeom g = x == 0 ? tg[0] : tg[NT - 1];          // this CTA's rows
     const int rpos = ctx0 + g.t0 + r / G;                    // position of this row's query
     const int rpos_warp = ctx0 + g.t0 + (r & ~31) / G;       // smallest position in the warp
     const float sc = p.scale_log2;
@@ -485,7 +560,7 @@ __global__ void __launch_bounds__(384, 1)
     // V tile 0 before the first step, then tile j+1 after step j
     if (n_kv > 0 && vt >= 0 && !convert_v(0)) ok = false;
     for (int j = 0; j < g.n_kv && ok; ++j) {
-      if (!mbar_wait(smem_addr(s_full + x), j & 1)) { ok = false; break; }
+      if (!wait(s_full + x, j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       const int kp0 = j * BN;
       const bool full = kp0 + BN - 1 <= rpos_warp;  // below the diagonal for the whole warp
@@ -498,14 +573,18 @@ __global__ void __launch_bounds__(384, 1)
       // row maximum of scale * S over the visible positions
       float mx;
       if (full && sc > 0.f) {
+        // four independent chains of three-input maxima: half the instructions of a
+        // two-input chain (every instruction of these warps competes for issue slots
+        // with the MMA-issuing thread on one of the four schedulers)
         float rm[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           rm[k] = c[k][0];
 #pragma unroll
-          for (int i = 1; i < 32; ++i) rm[k] = fmaxf(rm[k], c[k][i]);
+          for (int i = 1; i < 31; i += 2) rm[k] = fmax3f(rm[k], c[k][i], c[k][i + 1]);
+          rm[k] = fmaxf(rm[k], c[k][31]);
         }
-        mx = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3])) * sc;
+        mx = fmax3f(rm[0], rm[1], fmaxf(rm[2], rm[3])) * sc;
       } else if (full) {
         mx = kNegInf;
 #pragma unroll
@@ -549,7 +628,7 @@ __global__ void __launch_bounds__(384, 1)
       l = l * alpha + ((s2[0] + s2[1]) + (s2[2] + s2[3]));
       if (j >= 1 && __any_sync(~0u, need)) {
         // O holds P_0..j-1 V: once the last of those products is done, rescale it
-        if (!mbar_wait(smem_addr(pv_done + x), (j - 1) & 1)) { ok = false; break; }
+        if (!wait(pv_done + x, (j - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -563,11 +642,12 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(smem_addr(p_full + x));
+      __syncwarp();
+      if (lane == 0) arrive_lead(p_full + x);
       if (j + 1 < n_kv && vt >= 0 && !convert_v(j + 1)) { ok = false; break; }
     }
-    // the CTA's K/V tiles past this tile's last (the other tile reaches further) still
-    // need this warpgroup's half of their conversion
+    // the item's K/V tiles past this tile's last (the other tile reaches further) still
+    // need this warpgroup's share of their conversion
     for (int jv = g.n_kv + 1; jv < n_kv && ok && vt >= 0; ++jv)
       if (!convert_v(jv)) ok = false;
     if constexpr (Fmt<T>::v == 1) {
@@ -576,7 +656,7 @@ __global__ void __launch_bounds__(384, 1)
       if (!(vm.x < 65504.5f && vm.y < 65504.5f)) flag_status(p.status, PA_STATUS_RANGE);
     }
     // epilogue: O / l -> out rows
-    if (ok && g.n_kv > 0 && mbar_wait(smem_addr(pv_done + x), (g.n_kv - 1) & 1)) {
+    if (ok && g.n_kv > 0 && wait(pv_done + x, (g.n_kv - 1) & 1)) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
       const int rows_valid = g.ntok * G;
@@ -612,19 +692,24 @@ __global__ void __launch_bounds__(384, 1)
   }
   griddep_launch_dependents();
   tc::fence_before_sync();
-  __syncthreads();
+  // in a pair, neither CTA frees its tensor memory or leaves while the other may still
+  // write into it or into its barriers
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (PAIR) tc::tmem_dealloc_pair(tmem, C::kTmemCols);
+    else tc::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 // ----------------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------------
-// Upper bound on the work items of a call: every sequence's chunk at its maximum.
-long long prefill_max_items(int num_seqs, int max_q, int num_q_heads, int num_kv_heads) {
-  const long long rows_per_item = 128 * 2;  // PrefillCfg<>::BM * kTiles
+// Upper bound on the work items of a call: every sequence's chunk at its maximum, in
+// items of `rows_per_item` query rows (256 for one CTA, 512 for a pair).
+long long prefill_max_items(int num_seqs, int max_q, int num_q_heads, int num_kv_heads,
+                            int rows_per_item = 256) {
   const long long per_seq = ((long long)max_q * (num_q_heads / num_kv_heads) + rows_per_item - 1) /
                             rows_per_item;
   return (long long)num_seqs * num_kv_heads * per_seq;
@@ -634,7 +719,10 @@ std::mutex g_mutex;
 
 template <typename T, int D, int BS>
 int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
-  using C = PrefillCfg<D, BS>;
+  // head dim 128: CTA pairs; head dim 64 (a V half of 32 columns per CTA would not fill
+  // a 128-byte swizzle row): one CTA per product
+  constexpr bool kPair = D == 128;
+  using C = PrefillCfg<D, BS, kPair>;
   static bool configured[kMaxDev] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDev)
@@ -642,7 +730,7 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(prefill_kernel<T, D, BS>,
+      if (cudaFuncSetAttribute(prefill_kernel<T, D, BS, kPair>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)C::kSmem) != cudaSuccess)
         return fail(PA_ERR_CUDA, "pa_prefill_chunk: shared-memory configuration failed");
@@ -673,8 +761,11 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   p.num_blocks = a.num_blocks;
   p.out_f32 = a.out_dtype == PA_F32;
   p.scale_log2 = a.scale * kLog2e;
-  const long long items = prefill_max_items(a.num_seqs, a.max_q, a.num_q_heads, a.num_kv_heads);
-  if (items > 0x7fffffffll) return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: grid too large");
+  const int rows_per_item = C::BM * C::kTiles * C::kCtas;
+  const long long items = prefill_max_items(a.num_seqs, a.max_q, a.num_q_heads, a.num_kv_heads,
+                                            rows_per_item);
+  if (items * C::kCtas > 0x7fffffffll)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: grid too large");
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.header = reinterpret_cast<int*>(ws);
   p.items = reinterpret_cast<const PrefillItem*>(ws + 256);
@@ -682,13 +773,13 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   while (((long long)a.max_ctx / C::BN + 1) >> key_shift >= kPlanBuckets) ++key_shift;
   cudaError_t e = launch_pdl(prefill_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream,
                              a.cu_q_lens, a.context_lens, a.num_seqs, a.num_kv_heads, G,
-                             C::BM * C::kTiles, C::BN, key_shift,
+                             rows_per_item, C::BN, key_shift,
                              std::min<long long>(a.max_ctx, (long long)a.max_blocks * a.block_size),
                              reinterpret_cast<PrefillItem*>(ws + 256), reinterpret_cast<int*>(ws),
                              a.status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_prefill_chunk (plan): %s", cudaGetErrorString(e));
-  e = launch_pdl(prefill_kernel<T, D, BS>, dim3((unsigned)items), dim3(C::kThreads), C::kSmem,
-                 stream, tmq, tmk, tmv, p);
+  e = launch_pdl_cluster(prefill_kernel<T, D, BS, kPair>, dim3((unsigned)(items * C::kCtas)),
+                         dim3(C::kThreads), C::kSmem, stream, C::kCtas, tmq, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_prefill_chunk: %s", cudaGetErrorString(e));
   return PA_OK;
 }
