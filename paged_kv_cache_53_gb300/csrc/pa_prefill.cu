@@ -99,9 +99,10 @@ struct PrefillCfg {
   static constexpr int kVReadyArrivals = kVThreads / 32 * kCtas;
   static constexpr int kPFullArrivals = 4 * kCtas;
   // barriers: q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], v_ready[SV], then
-  // per query tile s_full, p_full, pv_done.  K(j) is done with once S(j) has been
-  // computed, an iteration before P(j) V(j), so the next K tile loads that much earlier.
-  static constexpr int kBars = 1 + 2 * kKStages + 3 * kVStages + 3 * kTiles;
+  // per query tile s_full, p_full (first 64 tokens of P), p_full2 (the other 64),
+  // pv_done.  K(j) is done with once S(j) has been computed, an iteration before P(j)
+  // V(j), so the next K tile loads that much earlier.
+  static constexpr int kBars = 1 + 2 * kKStages + 3 * kVStages + 4 * kTiles;
   static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + kKStages * (size_t)kKBytes +
                                   kVStages * (size_t)kVBytes + kBars * 8 + 16;
 };
@@ -243,8 +244,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* v_empty = v_full + SV;
   uint64_t* v_ready = v_empty + SV;      // V of the stage converted to fp16
   uint64_t* s_full = v_ready + SV;       // [tile]
-  uint64_t* p_full = s_full + NT;
-  uint64_t* pv_done = p_full + NT;
+  uint64_t* p_full = s_full + NT;        // [tile] P's first half published
+  uint64_t* p_full2 = p_full + NT;       // [tile] its second half
+  uint64_t* pv_done = p_full2 + NT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int x = 0; x < NT; ++x) {
       mbar_init(smem_addr(s_full + x), 1);
       mbar_init(smem_addr(p_full + x), C::kPFullArrivals);
+      mbar_init(smem_addr(p_full2 + x), C::kPFullArrivals);
       mbar_init(smem_addr(pv_done + x), 1);
     }
     fence_mbar_init();
@@ -487,6 +490,7 @@ __global__ void __launch_bounds__(384, 1)
         commit(s_full + x);
       };
       int v_seen = -1;  // last K/V tile whose fp16 V was waited for
+      // P_x(j) V(j), in two halves of 64 tokens as the softmax publishes them
       auto issue_pv = [&](int x, int j, int sv, uint32_t vpar) -> bool {
         if (!wait_w(p_full + x, j & 1)) return false;
         if (v_seen < j) {
@@ -498,9 +502,14 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tO = tmem + NT * BN + x * D;
         const uint64_t dv = tc::desc_advance(dv0, sv * C::kVBytes);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          if (ks == BN / 32) {
+            if (!wait_w(p_full2 + x, j & 1)) return false;
+            tc::fence_after_sync();
+          }
           tc::mma_ts_warp<PAIR>(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o,
                                 j > 0 || ks > 0);
+        }
         commit(pv_done + x);
         return true;
       };
@@ -605,8 +614,19 @@ __global__ void __launch_bounds__(384, 1)
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
+      // O holds P_0..j-1 V and must be rescaled before P_j V accumulates into it
+      const bool rescale = j >= 1 && __any_sync(~0u, need);
+      auto publish = [&](uint64_t* bar) {
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_lead(bar);
+      };
       // P = 2^(scale * S - m) in fp16, tokens 32k .. 32k+31 into columns 16k .. 16k+15
-      // (the scores there are already in registers)
+      // (the scores there are already in registers).  It is published in two halves of 64
+      // tokens (p_full, p_full2) so that the first half's P V products run while the
+      // second half is computed; a warp that must rescale O first publishes both halves
+      // after it.
       // exponent t = scale * S - m (the diagonal's scores are scaled already: factor 1),
       // two columns per packed FMA (each lane rounds as a scalar fmaf would)
       const float f = full ? sc : 1.f;
@@ -624,10 +644,11 @@ __global__ void __launch_bounds__(384, 1)
           pk[i] = Mma<__half>::pack(e0, e1);
         }
         tc::tmem_st16(tS + 16 * k, pk);
+        if ((k & 1) && !rescale) publish(k == 1 ? p_full + x : p_full2 + x);
       }
       l = l * alpha + ((s2[0] + s2[1]) + (s2[2] + s2[3]));
-      if (j >= 1 && __any_sync(~0u, need)) {
-        // O holds P_0..j-1 V: once the last of those products is done, rescale it
+      if (rescale) {
+        // once the last of P_0..j-1 V is done
         if (!wait(pv_done + x, (j - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
 #pragma unroll
@@ -639,11 +660,9 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
           tc::tmem_st32(tO + c0, o);
         }
+        publish(p_full + x);
+        publish(p_full2 + x);
       }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) arrive_lead(p_full + x);
       if (j + 1 < n_kv && vt >= 0 && !convert_v(j + 1)) { ok = false; break; }
     }
     // the item's K/V tiles past this tile's last (the other tile reaches further) still
