@@ -226,68 +226,80 @@ __global__ void __launch_bounds__(384, 1)
     if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... as in the chunked-prefill kernel
-    if (lane == 0) {
+    // PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... as in the chunked-prefill kernel.  The
+    // whole warp runs the loop (waits included, so that it never diverges) and one elected
+    // lane issues each MMA and commit: few instructions per MMA for a warp that shares its
+    // scheduler with two softmax warps.
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(~0u, mbar_wait(smem_addr(bar), parity));
+      };
       const uint32_t id_s = tc::idesc_f16(SpFmt<T>::v, C::BM, BN, false, false);
       const uint32_t id_o = tc::idesc_f16(SpFmt<T>::v, C::BM, D, false, true);
-      // descriptors of each operand's first k-step, advanced by constant offsets (fewer
-      // instructions per MMA for a thread that shares its scheduler with softmax warps)
-      uint64_t dq[NT];
-#pragma unroll
-      for (int x = 0; x < NT; ++x) dq[x] = tc::smem_desc_sw128(smem_addr(sQ + x * C::kQBytes), 16, 1024);
-      auto issue_s = [&](int x, int j) {
+      // descriptors of each operand's first k-step and first stage, advanced by constant
+      // offsets
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(sKV), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sKV + C::kKBytes), C::kKvHalfBytes, 1024);
+      auto issue_s = [&](int x, int s) {
         const uint32_t tS = tmem + x * BN;
-        const uint64_t dk = tc::smem_desc_sw128(smem_addr(sKV + (j % S) * C::kStageBytes), 16, 1024);
+        const uint64_t dq = tc::desc_advance(dq0, x * C::kQBytes);
+        const uint64_t dk = tc::desc_advance(dk0, s * C::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          tc::mma_f16_ss(tS, tc::desc_advance(dq[x], (kk >> 2) * C::kQHalfBytes + koff),
-                         tc::desc_advance(dk, (kk >> 2) * C::kKvHalfBytes + koff), id_s, kk > 0);
+          tc::mma_ss_warp<false>(tS, tc::desc_advance(dq, (kk >> 2) * C::kQHalfBytes + koff),
+                                 tc::desc_advance(dk, (kk >> 2) * C::kKvHalfBytes + koff), id_s,
+                                 kk > 0);
         }
-        tc::commit(smem_addr(s_full + x));
+        tc::commit_warp<false>(smem_addr(s_full + x));
       };
-      auto issue_pv = [&](int x, int j) -> bool {
-        if (!mbar_wait(smem_addr(p_full + x), j & 1)) return false;
+      auto issue_pv = [&](int x, int j, int s) -> bool {
+        if (!wait_w(p_full + x, j & 1)) return false;
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint64_t dv = tc::smem_desc_sw128(
-            smem_addr(sKV + (j % S) * C::kStageBytes + C::kKBytes), C::kKvHalfBytes, 1024);
+        const uint64_t dv = tc::desc_advance(dv0, s * C::kStageBytes);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
           const uint64_t bdesc = tc::desc_advance(dv, ks * 16 * 128);
-          tc::mma_f16_ts(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
-          tc::mma_f16_ts(tO, tP + col + 16, bdesc, id_o, true);
+          tc::mma_ts_warp<false>(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
+          tc::mma_ts_warp<false>(tO, tP + col + 16, bdesc, id_o, true);
         }
-        tc::commit(smem_addr(pv_done + x));
+        tc::commit_warp<false>(smem_addr(pv_done + x));
         return true;
       };
-      if (!mbar_wait(smem_addr(q_full), 0) || !mbar_wait(smem_addr(kv_full), 0)) ok = false;
+      if (!wait_w(q_full, 0) || !wait_w(kv_full, 0)) ok = false;
       if (ok) {
         tc::fence_after_sync();
 #pragma unroll
         for (int x = 0; x < NT; ++x)
           if (valid[x]) issue_s(x, 0);
       }
+      // stage of step j and of step j + 1 (with its phase parity), without divisions
+      int s = 0, s1 = S > 1 ? 1 : 0;
+      uint32_t par1 = S > 1 ? 0 : 1;
       for (int j = 0; j < n_kv && ok; ++j) {
         bool next_ready = false;
 #pragma unroll
         for (int x = 0; x < NT; ++x) {
           if (!valid[x]) continue;
-          if (!issue_pv(x, j)) { ok = false; break; }
+          if (!issue_pv(x, j, s)) { ok = false; break; }
           if (j + 1 < n_kv) {
             if (!next_ready) {
-              if (!mbar_wait(smem_addr(kv_full + (j + 1) % S), ((j + 1) / S) & 1)) { ok = false; break; }
+              if (!wait_w(kv_full + s1, par1)) { ok = false; break; }
               tc::fence_after_sync();
               next_ready = true;
             }
-            issue_s(x, j + 1);
+            issue_s(x, s1);
           }
         }
-        tc::commit(smem_addr(kv_empty + j % S));
+        tc::commit_warp<false>(smem_addr(kv_empty + s));
+        if (++s == S) s = 0;
+        if (++s1 == S) { s1 = 0; par1 ^= 1; }
       }
-      if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
+      if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (warp >= 4) {
