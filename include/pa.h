@@ -66,8 +66,8 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 #define PA_STATUS_BAD_SLOT 0x2    /* a slot outside [0, num_blocks * block_size) */
 #define PA_STATUS_BAD_CONTEXT 0x4 /* context < 0, or longer than max_ctx / its table */
 #define PA_STATUS_TIMEOUT 0x8     /* a pipeline wait in a kernel gave up (never expected) */
-#define PA_STATUS_RANGE 0x10      /* chunked prefill met a bf16 V value of magnitude >= 65520,
-                                     outside fp16's range (see pa_prefill_chunk) */
+#define PA_STATUS_RANGE 0x10      /* reserved: no longer set (pa_prefill_chunk computes V
+                                     values outside fp16's range exactly) */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pa_version(void);
@@ -376,8 +376,10 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int max_q, int n
  * QK^T and PV run on the tensor cores with fp32 accumulation.  P and V enter the PV
  * product in fp16 (unit roundoff 2^-11; bf16's 2^-8 alone would not meet a 2e-3 bound):
  * bf16 V values are converted to fp16 in shared memory, which is exact for magnitudes
- * from 2^-14 up to 65520 (below 2^-14 they become fp16 subnormals, within 2^-25); a V
- * value of 65520 or more sets PA_STATUS_RANGE (its products are not exact).
+ * from 2^-14 up to 65520 (below 2^-14 they become fp16 subnormals, within 2^-25).  The
+ * work items (sequence, KV head, group of query rows) that meet a V value of 65520 or
+ * more are computed again in the same call with V in bf16 and P as two bf16 terms (hi +
+ * lo, a relative error of at most 2^-18 per probability), as pa_decode computes them.
  */
 int pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
                      const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,

@@ -32,7 +32,7 @@ __all__ = [
 
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 STATUS_BAD_BLOCK, STATUS_BAD_SLOT, STATUS_BAD_CONTEXT, STATUS_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-STATUS_RANGE = 0x10
+STATUS_RANGE = 0x10  # reserved: no longer set
 _ERRORS = {1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
            4: "PA_ERR_CUDA"}
 

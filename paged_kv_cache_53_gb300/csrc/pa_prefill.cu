@@ -52,8 +52,8 @@ struct PrefillItem;
 
 struct PrefillParams {
   void* out;
-  const PrefillItem* items;
-  const int* header;
+  PrefillItem* items;  // the work list; the main pass marks items for the exact pass
+  int* header;         // [0] items, [1] 1 once any item is marked
   const int32_t* block_tables;
   const int32_t* cu_q_lens;
   const int32_t* context_lens;
@@ -118,17 +118,13 @@ struct Fmt<__nv_bfloat16> {
   static constexpr int v = 1;
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
 
 // ----------------------------------------------------------------------------------
 // plan: one work item per (sequence, KV head, pair of query tiles), heaviest first
 // ----------------------------------------------------------------------------------
 struct PrefillItem {
-  int b, h, ctile, pad;
+  int b, h, ctile;
+  int wide;  // set by the main pass: a V value of the item is outside fp16's range
 };
 
 constexpr int kPlanBuckets = 4096;
@@ -193,7 +189,10 @@ __global__ void __launch_bounds__(kPlanThreads)
       if (lane >= o) iw += t;
     }
     s_warp[lane] = iw - w;
-    if (lane == 31) header[0] = iw;
+    if (lane == 31) {
+      header[0] = iw;
+      header[1] = 0;
+    }
   }
   __syncthreads();
   int off = s_warp[wid] + incl - run;
@@ -222,10 +221,18 @@ struct TileGeom {
   int n_kv;     // K/V tiles it needs (0 if ntok == 0)
 };
 
-template <typename T, int D, int BS, bool PAIR>
-__global__ void __launch_bounds__(384, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+// One work item (sequence, KV head, group of query tiles) by one CTA or CTA pair.
+// WIDE: the exact pass for items whose V holds values outside fp16's range (bf16 caches
+// only): V stays bf16 in shared memory and P enters P V as bf16 hi + lo terms (a relative
+// error of 2^-17, as in decode), twice the P V products.
+template <typename T, int D, int BS, bool PAIR, bool WIDE>
+__device__ __forceinline__ void prefill_item(const CUtensorMap& tmq, const CUtensorMap& tmk,
+                                             const CUtensorMap& tmv, const PrefillParams& p,
+                                             int it) {
+  // a CTA that runs one item (the main pass) gives up the right to allocate tensor memory
+  // once it has its columns; the exact pass allocates once per item it takes
+  constexpr bool relinquish = !WIDE;
+  static_assert(!WIDE || Fmt<T>::v == 1, "the exact pass is for bf16 caches");
   using C = PrefillCfg<D, BS, PAIR>;
   constexpr int BN = C::BN, SK = C::kKStages, SV = C::kVStages, NT = C::kTiles, NC = C::kCtas;
   static_assert(C::kSmem <= 232448, "shared memory per CTA");
@@ -237,6 +244,9 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sV = sK + SK * C::kKBytes;              // [V stage][half][128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kVBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
+  // set by a converting thread that met a V value outside fp16's range; read once the
+  // item is done
+  volatile uint32_t* wide_flag = tmem_slot + 1;
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* k_empty = k_full + SK;
@@ -269,10 +279,7 @@ __global__ void __launch_bounds__(384, 1)
     else mbar_arrive(smem_addr(bar));
   };
 
-  griddep_wait();  // the work list and the chunk's K/V (cache write) are complete
   // every exit before the barriers are set up is taken by both CTAs of a pair together
-  const int it = (int)blockIdx.x / NC;
-  if (it >= __ldg(p.header)) return;  // more CTAs launched than items
   const PrefillItem item = p.items[it];
   const int h = item.h, b = item.b;
   const int q_begin = __ldg(p.cu_q_lens + b);
@@ -301,6 +308,7 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = pg[NT - 1].ntok > 0 ? pg[NT - 1].n_kv : pg[0].n_kv;  // the item's K/V tiles
 
   if (threadIdx.x == 0) {
+    *wide_flag = 0;
     mbar_init(smem_addr(q_full), 1);
     for (int i = 0; i < SK; ++i) {
       mbar_init(smem_addr(k_full + i), 1);
@@ -322,10 +330,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 1) {
     if constexpr (PAIR) {
       tc::tmem_alloc_pair(smem_addr(tmem_slot), C::kTmemCols);
-      tc::tmem_relinquish_pair();
+      if constexpr (relinquish) tc::tmem_relinquish_pair();
     } else {
       tc::tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
-      tc::tmem_relinquish();
+      if constexpr (relinquish) tc::tmem_relinquish();
     }
   }
   if (threadIdx.x == 32 + 1) {
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(384, 1)
       const int i = vt + u * C::kVThreads;
       if (z0 < BN && ((i % (C::kVHalfBytes / 16)) >> 3) >= z0) {
         v[u] = make_uint4(0, 0, 0, 0);
-      } else if constexpr (Fmt<T>::v == 1) {
+      } else if constexpr (Fmt<T>::v == 1 && !WIDE) {
         uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -469,7 +477,8 @@ __global__ void __launch_bounds__(384, 1)
         return __all_sync(~0u, wait(bar, parity));
       };
       const uint32_t id_s = tc::idesc_f16(Fmt<T>::v, C::BM * NC, BN, false, false);
-      const uint32_t id_o = tc::idesc_f16(Fmt<__half>::v, C::BM * NC, D, false, true);  // fp16 P, V
+      // fp16 P and V; bf16 hi + lo P and bf16 V in the exact pass
+      const uint32_t id_o = tc::idesc_f16(WIDE ? Fmt<T>::v : Fmt<__half>::v, C::BM * NC, D, false, true);
       auto commit = [](uint64_t* bar) { tc::commit_warp<PAIR>(smem_addr(bar)); };
       // descriptors of each operand's first k-step and first stage, advanced by constant
       // offsets below
@@ -509,6 +518,9 @@ __global__ void __launch_bounds__(384, 1)
           }
           tc::mma_ts_warp<PAIR>(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o,
                                 j > 0 || ks > 0);
+          if constexpr (WIDE)  // the lo terms, in columns 64 .. 127
+            tc::mma_ts_warp<PAIR>(tO, tP + 64 + 8 * ks, tc::desc_advance(dv, ks * 16 * 128),
+                                  id_o, true);
         }
         commit(pv_done + x);
         return true;
@@ -549,9 +561,13 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 2 || warp == 3) {
     for (int jv = 0; jv < n_kv && ok; ++jv)
       if (!convert_v(jv)) ok = false;
-    if constexpr (Fmt<T>::v == 1) {
+    if constexpr (Fmt<T>::v == 1 && !WIDE) {
+      // a value at or above 65520 in magnitude became inf (NaN stays NaN): the item is
+      // computed again by the exact pass
       const float2 vm = __half22float2(vmax);
-      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) flag_status(p.status, PA_STATUS_RANGE);
+      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) {
+        *wide_flag = 1;
+      }
     }
     if (!ok) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp >= 4) {
@@ -641,9 +657,21 @@ __global__ void __launch_bounds__(384, 1)
           f2_split(f2_fma(f2(c[k][2 * i], c[k][2 * i + 1]), f2x, negm2), t0, t1);
           const float e0 = fast_exp2(t0), e1 = fast_exp2(t1);
           s2[i & 3] += e0 + e1;
-          pk[i] = Mma<__half>::pack(e0, e1);
+          if constexpr (WIDE) {
+            uint32_t lo;
+            pk[i] = Mma<T>::pack_split(e0, e1, lo);
+            c[k][i] = __uint_as_float(lo);  // the scores of this chunk are spent
+          } else {
+            pk[i] = Mma<__half>::pack(e0, e1);
+          }
         }
         tc::tmem_st16(tS + 16 * k, pk);
+        if constexpr (WIDE) {
+          uint32_t lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lo[i] = __float_as_uint(c[k][i]);
+          tc::tmem_st16(tS + 64 + 16 * k, lo);
+        }
         if ((k & 1) && !rescale) publish(k == 1 ? p_full + x : p_full2 + x);
       }
       l = l * alpha + ((s2[0] + s2[1]) + (s2[2] + s2[3]));
@@ -669,10 +697,13 @@ __global__ void __launch_bounds__(384, 1)
     // need this warpgroup's share of their conversion
     for (int jv = g.n_kv + 1; jv < n_kv && ok && vt >= 0; ++jv)
       if (!convert_v(jv)) ok = false;
-    if constexpr (Fmt<T>::v == 1) {
-      // a value at or above 65520 in magnitude became inf (NaN stays NaN): flag it
+    if constexpr (Fmt<T>::v == 1 && !WIDE) {
+      // a value at or above 65520 in magnitude became inf (NaN stays NaN): the item is
+      // computed again by the exact pass
       const float2 vm = __half22float2(vmax);
-      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) flag_status(p.status, PA_STATUS_RANGE);
+      if (!(vm.x < 65504.5f && vm.y < 65504.5f)) {
+        *wide_flag = 1;
+      }
     }
     // epilogue: O / l -> out rows
     if (ok && g.n_kv > 0 && wait(pv_done + x, (g.n_kv - 1) & 1)) {
@@ -720,6 +751,43 @@ __global__ void __launch_bounds__(384, 1)
     if constexpr (PAIR) tc::tmem_dealloc_pair(tmem, C::kTmemCols);
     else tc::tmem_dealloc(tmem, C::kTmemCols);
   }
+  if constexpr (Fmt<T>::v == 1 && !WIDE) {
+    // the item is computed again by the exact pass (either CTA of a pair may mark it)
+    if (threadIdx.x == 0 && *wide_flag != 0) {
+      p.items[it].wide = 1;
+      p.header[1] = 1;
+    }
+  }
+}
+
+// The main pass: CTA (pair) i takes item i.
+template <typename T, int D, int BS, bool PAIR>
+__global__ void __launch_bounds__(384, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+  griddep_wait();  // the work list and the chunk's K/V (cache write) are complete
+  const int it = (int)blockIdx.x / PrefillCfg<D, BS, PAIR>::kCtas;
+  if (it >= __ldg(p.header)) return;  // more CTAs launched than items
+  prefill_item<T, D, BS, PAIR, false>(tmq, tmk, tmv, p, it);
+}
+
+// The exact pass (bf16 caches), launched after the main pass: one wave of CTAs (pairs),
+// each looping over the items; all leave at once unless the main pass marked an item.
+template <typename T, int D, int BS, bool PAIR>
+__global__ void __launch_bounds__(384, 1)
+    prefill_wide_kernel(const __grid_constant__ CUtensorMap tmq,
+                        const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+  constexpr int NC = PrefillCfg<D, BS, PAIR>::kCtas;
+  griddep_wait();  // the main pass is complete, its marks written
+  if (__ldcg(p.header + 1) == 0) {
+    griddep_launch_dependents();
+    return;
+  }
+  const int n = __ldcg(p.header);
+  for (int it = (int)blockIdx.x / NC; it < n; it += (int)gridDim.x / NC)
+    if (__ldcg(&p.items[it].wide) != 0) prefill_item<T, D, BS, PAIR, true>(tmq, tmk, tmv, p, it);
+  griddep_launch_dependents();
 }
 
 // ----------------------------------------------------------------------------------
@@ -749,10 +817,14 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(prefill_kernel<T, D, BS, kPair>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)C::kSmem) != cudaSuccess)
-        return fail(PA_ERR_CUDA, "pa_prefill_chunk: shared-memory configuration failed");
+      bool ok = cudaFuncSetAttribute(prefill_kernel<T, D, BS, kPair>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)C::kSmem) == cudaSuccess;
+      if constexpr (Fmt<T>::v == 1)
+        ok = ok && cudaFuncSetAttribute(prefill_wide_kernel<T, D, BS, kPair>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)C::kSmem) == cudaSuccess;
+      if (!ok) return fail(PA_ERR_CUDA, "pa_prefill_chunk: shared-memory configuration failed");
       configured[dev] = true;
     }
   }
@@ -787,7 +859,7 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
     return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk: grid too large");
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.header = reinterpret_cast<int*>(ws);
-  p.items = reinterpret_cast<const PrefillItem*>(ws + 256);
+  p.items = reinterpret_cast<PrefillItem*>(ws + 256);
   int key_shift = 0;
   while (((long long)a.max_ctx / C::BN + 1) >> key_shift >= kPlanBuckets) ++key_shift;
   cudaError_t e = launch_pdl(prefill_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream,
@@ -800,6 +872,15 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   e = launch_pdl_cluster(prefill_kernel<T, D, BS, kPair>, dim3((unsigned)(items * C::kCtas)),
                          dim3(C::kThreads), C::kSmem, stream, C::kCtas, tmq, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_prefill_chunk: %s", cudaGetErrorString(e));
+  if constexpr (Fmt<T>::v == 1) {
+    // bf16: the exact pass for items whose V does not fit fp16 (one wave, idle otherwise)
+    const long long wave = std::max(1, sm_count() / C::kCtas);
+    const long long n = std::min<long long>(items, wave) * C::kCtas;
+    e = launch_pdl_cluster(prefill_wide_kernel<T, D, BS, kPair>, dim3((unsigned)n),
+                           dim3(C::kThreads), C::kSmem, stream, C::kCtas, tmq, tmk, tmv, p);
+    if (e != cudaSuccess)
+      return fail(PA_ERR_CUDA, "pa_prefill_chunk (exact pass): %s", cudaGetErrorString(e));
+  }
   return PA_OK;
 }
 

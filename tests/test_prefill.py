@@ -102,19 +102,62 @@ def test_prefill_nan_past_context_is_ignored(pa):
     assert max_abs_err(got, ref["out_prefill"]) <= TOL["bf16"]
 
 
-def test_prefill_v_beyond_fp16_range_is_flagged(pa):
-    """P V runs in fp16: a bf16 V value of magnitude >= 65520 cannot be converted exactly
-    and sets the range status bit; values just inside fp16's range stay exact."""
-    step = W.prefill_step("prange", W.Shape(8, 2, 128, 16, "bf16"), [40], [8], seed=36)
+# Bound for V values outside fp16's range, which the exact pass takes with P as bf16 hi +
+# lo terms: each probability is carried to a relative error of at most 2^-18, so the
+# output moves by at most 2^-18 * max|v| (fp32 sums add less); 2^-16 leaves a margin of 4.
+def _wide_tol(v_abs_max: float) -> float:
+    return TOL["bf16"] + 2.0 ** -16 * v_abs_max
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_v_beyond_fp16_range_is_exact(pa, d):
+    """P V runs in fp16 with V converted from bf16; a V value of magnitude >= 65520 does not
+    fit, and the work items that meet one are computed again with V in bf16 and P as hi +
+    lo terms.  Outputs must match the oracle (no status bit: nothing is flagged)."""
+    step = W.prefill_step("prange", W.Shape(8, 2, d, 16, "bf16"), [40, 300], [8, 200],
+                          seed=36)
     run = StepRun(step)
-    blk = int(step.prefill.block_tables[0, 0])
-    run.vals["v_cache"][blk, 0, 3, 5] = 65280.0  # the largest bf16 below 65520
-    run.run()
+    b = step.prefill
+    # large values in sequence 0's first block (KV head 1) and in sequence 1's context
+    blk0 = int(b.block_tables[0, 0])
+    run.vals["v_cache"][blk0, 1, 2, 7] = -1.0e5
+    run.vals["v_cache"][blk0, 1, 5, 0] = 3.0e6
+    blk1 = int(b.block_tables[1, 3])
+    run.vals["v_cache"][blk1, 0, 9, 11] = 7.0e4
+    kc, vc = run.host_pool()
+    vals = run.host_values()
+    res = run.run()
+    assert pa.get_status() == 0
+    ref = oracle_step(step, kc, vc, vals)
+    got = to_f64(res["out_prefill"])
+    assert np.isfinite(got).all()
+    assert max_abs_err(got, ref["out_prefill"]) <= _wide_tol(3.0e6)
+
+
+def test_prefill_exact_pass_touches_only_marked_items(pa):
+    """Only the work items whose V holds an out-of-range value are computed again: the
+    other sequence's outputs equal those of a run without any such value, bit for bit;
+    values just inside fp16's range stay on the fast path."""
+    shape = W.Shape(32, 8, 128, 32, "bf16")
+    step = W.prefill_step("pmark", shape, [600, 700], [300, 200], seed=38)
+    clean = StepRun(step)
+    blk = int(step.prefill.block_tables[1, 2])
+    clean.vals["v_cache"][blk, 3, 1, 2] = 65280.0  # the largest bf16 below 65520
+    out_clean = clean.run()["out_prefill"]
     assert pa.get_status() == 0
     run = StepRun(step)
-    run.vals["v_cache"][blk, 1, 2, 7] = -1.0e5
-    run.run()
-    assert pa.get_status() & pa.STATUS_RANGE
+    run.vals["v_cache"][blk, 3, 1, 2] = 65280.0
+    blk0 = int(step.prefill.block_tables[0, 1])
+    run.vals["v_cache"][blk0, 5, 4, 100] = -2.5e5
+    kc, vc = run.host_pool()
+    vals = run.host_values()
+    out = run.run()["out_prefill"]
+    assert pa.get_status() == 0
+    n0 = int(step.prefill.query_lens[0])
+    assert torch.equal(out[n0:], out_clean[n0:])
+    ref = oracle_step(step, kc, vc, vals)
+    got = to_f64(out)
+    assert max_abs_err(got, ref["out_prefill"]) <= _wide_tol(2.5e5)
 
 
 def test_mixed_prefill_full_size_sampled(pa):
