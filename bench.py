@@ -583,6 +583,7 @@ def run_ours(args, rank, world, local_rank):
                "achieved": round(flops / (pre_ms * 1e-3) / 1e12, 1), "peak": tpeak,
                "peak_kind": tkind, "unit": "TFLOP/s",
                "frac": round(flops / (pre_ms * 1e-3) / 1e12 / tpeak, 4),
+               "timing": "CUDA events around each call",
                "tokens": p.num_new_tokens, "max_ctx": p.max_ctx}
         config["prefill_tokens"] = p.num_new_tokens
     if d is not None:
@@ -592,7 +593,12 @@ def run_ours(args, rank, world, local_rank):
         alg = decode_algorithmic_bytes(step, out_dec.element_size(), shared=share)
         if fused_decode:  # the call also reads the new K/V rows, writes them and the slots
             alg += 2 * 2 * d.num_seqs * sh.num_kv_heads * sh.head_dim * sh.elem_bytes + 8 * d.num_seqs
-        achieved = alg / (dec_ms * 1e-3) / 1e9
+        # a step that is the decode call alone (no copies, no prefill): its back-to-back time
+        # is the call's duration as a serving loop sees it; the evented per-call time also
+        # carries the lost launch overlap an event between two calls costs
+        sole = p is None and pairs is None and fused_decode
+        launch_ms = step_ms if sole else dec_ms
+        achieved = alg / (launch_ms * 1e-3) / 1e9
         config.update({"num_seqs": d.num_seqs, "kv_tokens_per_step": kv_tokens,
                        "kv_bytes_per_step": kvb, "max_ctx": d.max_ctx,
                        "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV read per step "
@@ -627,7 +633,11 @@ def run_ours(args, rank, world, local_rank):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": None if share else recorded_traffic(args.workload),
                          "algorithmic_bytes": alg,
-                         "ms_per_launch": round(dec_ms, 5)},
+                         "ms_per_launch": round(launch_ms, 5),
+                         "ms_per_launch_evented": round(dec_ms, 5),
+                         "timing": ("back-to-back steps (the step is this one call), CUDA "
+                                    "events at the pass edges" if sole else
+                                    "CUDA events around each call")},
         })
         if p is not None:
             res["prefill"] = pre
@@ -677,25 +687,36 @@ def _device_inputs(step: W.Step, dev):
 
 
 def _time_call(call, seconds: float, stream, dev, per_pass: int = 20, warmup: int = 5):
-    """Mean device time of `call` (ms): passes of `per_pass` back-to-back calls with an
-    event pair around each, repeated until `seconds` have passed; clocks sampled meanwhile."""
+    """Device time of `call` (ms), in alternating passes of `per_pass` calls repeated until
+    `seconds` have passed, clocks sampled meanwhile: back-to-back passes with one event pair
+    around the whole pass (as a serving loop issues its calls: each call's first kernels
+    start while the previous call's last ones drain) give the median pass time per call;
+    evented passes, an event pair around each call (which ends that overlap), give the mean
+    per-call time.  Returns (back-to-back ms, evented ms, calls timed, clocks)."""
     import torch
     mk = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(warmup):
         call()
     torch.cuda.synchronize(dev)
     evs = [(mk(), mk()) for _ in range(per_pass)]
-    times = []
+    t0, t1 = mk(), mk()
+    times, passes = [], []
     with ClockSampler(dev.index or 0) as clocks:
         t_start = time.perf_counter()
         while not times or time.perf_counter() - t_start < seconds:
+            t0.record(stream)
+            for _ in range(per_pass):
+                call()
+            t1.record(stream)
             for a, b in evs:
                 a.record(stream)
                 call()
                 b.record(stream)
             torch.cuda.synchronize(dev)
+            passes.append(t0.elapsed_time(t1) / per_pass)
             times.extend(a.elapsed_time(b) for a, b in evs)
-    return float(np.mean(times)), len(times), clocks.summary()
+    return (float(np.median(passes)), float(np.mean(times)), len(times) + per_pass * len(passes),
+            clocks.summary())
 
 
 def run_extras(args, dev):
@@ -724,14 +745,14 @@ def run_extras(args, dev):
                                                         sh.num_q_heads, sh.num_kv_heads,
                                                         sh.head_dim, p.max_ctx, sh.block_size)),
                      dtype=torch.uint8, device=dev)
-    ms, n, clk = _time_call(lambda: pa.prefill_chunk(o, vals["q_prefill"], kc, vc, m["bt"],
+    ms, ms_ev, n, clk = _time_call(lambda: pa.prefill_chunk(o, vals["q_prefill"], kc, vc, m["bt"],
                                                      m["cu"], m["ctx"], p.max_q, p.max_ctx,
                                                      step.scale, ws), seconds, stream, dev)
     flops = prefill_useful_flops(step)
     tf = flops / (ms * 1e-3) / 1e12
     out["prefill_call"] = {
         "workload": step.name, "call": "pa_prefill_chunk", "ms_per_call": round(ms, 5),
-        "calls_timed": n, "clocks": clk,
+        "ms_per_call_evented": round(ms_ev, 5), "calls_timed": n, "clocks": clk,
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak,
                      "peak_kind": f"{tkind} bf16 dense, burst", "unit": "TFLOP/s",
                      "frac": round(tf / tpeak, 4), "frac_of_sustained": round(tf / tsus, 4),
@@ -753,7 +774,7 @@ def run_extras(args, dev):
     ws = torch.empty(pa.decode_shared_prefix_workspace_bytes(
         d.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, d.max_ctx, sh.block_size,
         len(sharers), plen), dtype=torch.uint8, device=dev)
-    ms, n, clk = _time_call(lambda: pa.decode_shared_prefix(o, vals["q_decode"], kc, vc, m["bt"],
+    ms, ms_ev, n, clk = _time_call(lambda: pa.decode_shared_prefix(o, vals["q_decode"], kc, vc, m["bt"],
                                                             m["ctx"], d.max_ctx, pb_t, plen,
                                                             sh_t, step.scale, ws),
                             seconds, stream, dev)
@@ -761,7 +782,7 @@ def run_extras(args, dev):
     gbs = alg / (ms * 1e-3) / 1e9
     out["shared_prefix_call"] = {
         "workload": step.name, "call": "pa_decode_shared_prefix", "ms_per_call": round(ms, 5),
-        "calls_timed": n, "clocks": clk,
+        "ms_per_call_evented": round(ms_ev, 5), "calls_timed": n, "clocks": clk,
         "logical_kv_gbs": round(kv_bytes(step) / (ms * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(gbs / hbm, 4),
@@ -779,7 +800,7 @@ def run_extras(args, dev):
     ws = torch.empty(pa.decode_workspace_bytes(d.num_seqs, sh.num_q_heads, sh.num_kv_heads,
                                                sh.head_dim, d.max_ctx, sh.block_size),
                      dtype=torch.uint8, device=dev)
-    ms, n, clk = _time_call(lambda: pa.decode_append(o, vals["q_decode"], vals["k_new_decode"],
+    ms, ms_ev, n, clk = _time_call(lambda: pa.decode_append(o, vals["q_decode"], vals["k_new_decode"],
                                                      vals["v_new_decode"], kc, vc, m["bt"],
                                                      m["ctx"], d.max_ctx, step.scale, ws),
                             seconds, stream, dev)
@@ -788,7 +809,7 @@ def run_extras(args, dev):
     gbs = alg / (ms * 1e-3) / 1e9
     out["opt13b_decode_call"] = {
         "workload": step.name, "call": "pa_decode_append", "ms_per_call": round(ms, 5),
-        "calls_timed": n, "clocks": clk,
+        "ms_per_call_evented": round(ms_ev, 5), "calls_timed": n, "clocks": clk,
         "kv_gbs": round(kv_bytes(step) / (ms * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(gbs / hbm, 4),
