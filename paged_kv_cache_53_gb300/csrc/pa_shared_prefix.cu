@@ -13,11 +13,16 @@
 // CTA (pair, split, h) owns two 128-row query tiles; row r of the pair is sharer
 // (pair * 256 + r) / G, query head h * G + r % G.  The pipeline is the chunked-prefill
 // kernel's: a TMA producer warp streams 128-token K/V tiles of the prefix through the
-// prefix's block list into a ring; one thread issues S = Q K^T and O += P V (P as hi +
-// lo 16-bit terms written into S's TMEM columns); two softmax warpgroups, one per query
-// tile, run the online softmax.  The query rows are gathered from scattered sequences,
-// so every thread of the CTA copies a share of them into 128-byte-swizzled shared memory
-// before the pipeline starts.  No causal mask: every row sees the whole split.
+// prefix's block list into a ring; one warp issues S = Q K^T and O += P V with P written
+// into S's TMEM columns; two softmax warpgroups, one per query tile, run the online
+// softmax.  The query rows are gathered from scattered sequences, so every thread of the
+// CTA copies a share of them into 128-byte-swizzled shared memory before the pipeline
+// starts.  No causal mask: every row sees the whole split.
+// P V: for fp16 caches P is one fp16 term (unit roundoff 2^-11) against V as stored; for
+// bf16 caches P is a pair of bf16 hi + lo terms (a relative error of 2^-17, twice the
+// products) against V as stored, bf16 having too few bits for P alone.  (Converting each
+// bf16 V tile to fp16 in place, by two warps, so that one fp16 P term would do, made
+// every step longer than the halved products saved.)
 #include <algorithm>
 #include <mutex>
 
@@ -46,6 +51,7 @@ struct SpCfg {
   static constexpr int kBlocksPerTile = BN / BS;
   static constexpr int kThreads = 384;
   static constexpr int kTmemCols = 512;
+  // kv_full[S], kv_empty[S], then per query tile s_full, p_full, pv_done, then q_full
   static constexpr int kBars = 2 * kStages + 3 * kTiles + 1;
   static constexpr int kGatherThreads = kThreads - 32;  // every warp but the producer
   static constexpr int kMaxSharers = kTiles * BM;  // sequences whose rows one CTA takes
@@ -260,12 +266,21 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
         const uint64_t dv = tc::desc_advance(dv0, s * C::kStageBytes);
+        if constexpr (SpFmt<T>::v == 0) {
+          // P: tokens 2c and 2c + 1 in column c
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
-          const uint64_t bdesc = tc::desc_advance(dv, ks * 16 * 128);
-          tc::mma_ts_warp<false>(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
-          tc::mma_ts_warp<false>(tO, tP + col + 16, bdesc, id_o, true);
+          for (int ks = 0; ks < BN / 16; ++ks)
+            tc::mma_ts_warp<false>(tO, tP + 8 * ks, tc::desc_advance(dv, ks * 16 * 128), id_o,
+                                   j > 0 || ks > 0);
+        } else {
+          // P of tokens 32k .. 32k+31: hi terms in columns 32k .. 32k+15, lo terms in the next 16
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
+            const uint64_t bdesc = tc::desc_advance(dv, ks * 16 * 128);
+            tc::mma_ts_warp<false>(tO, tP + col, bdesc, id_o, j > 0 || ks > 0);
+            tc::mma_ts_warp<false>(tO, tP + col + 16, bdesc, id_o, true);
+          }
         }
         tc::commit_warp<false>(smem_addr(pv_done + x));
         return true;
@@ -347,8 +362,11 @@ __global__ void __launch_bounds__(384, 1)
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
-      // P = 2^(scale * S - m) as hi + lo 16-bit terms over S's own columns; the next 32
-      // columns load while these are exponentiated
+      // P = 2^(scale * S - m) over S's own columns: for fp16, one term, tokens 32k .. 32k+31
+      // in columns 16k .. 16k+15 (their scores are already in registers); for bf16, hi + lo
+      // terms in columns 32k .. 32k+31.  The next 32 columns load while these are
+      // exponentiated.
+      constexpr bool wide = SpFmt<T>::v == 1;
       float sum = 0.f;
       {
         float buf[2][32];
@@ -373,16 +391,26 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < 32; ++i)
               a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
           }
-          uint32_t hi[16], lo[16];
           float s2[2] = {0.f, 0.f};
+          if constexpr (!wide) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            s2[i & 1] += a[2 * i] + a[2 * i + 1];
-            hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+            for (int i = 0; i < 16; ++i) {
+              s2[i & 1] += a[2 * i] + a[2 * i + 1];
+              pk[i] = Mma<__half>::pack(a[2 * i], a[2 * i + 1]);
+            }
+            tc::tmem_st16(tS + 16 * k, pk);
+          } else {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              s2[i & 1] += a[2 * i] + a[2 * i + 1];
+              hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+            }
+            tc::tmem_st16(tS + c0, hi);
+            tc::tmem_st16(tS + c0 + 16, lo);
           }
           sum += s2[0] + s2[1];
-          tc::tmem_st16(tS + c0, hi);
-          tc::tmem_st16(tS + c0 + 16, lo);
           if (k + 1 < BN / 32) tc::tmem_wait_ld();
         }
       }

@@ -90,6 +90,36 @@ def test_prefix_lengths(pa, prefix):
     _check(pa, step)
 
 
+# Bound for large V values: P enters P V as bf16 hi + lo terms, each probability carried to
+# a relative error of at most 2^-18, so the output moves by at most 2^-18 * max|v| (fp32
+# sums add less); 2^-16 leaves a margin of 4.
+def _wide_tol(v_abs_max: float) -> float:
+    return TOL["bf16"] + 2.0 ** -16 * v_abs_max
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_v_beyond_fp16_range_in_the_prefix(pa, d):
+    """bf16 prefix V values far outside fp16's range (and one just inside it, 65280, the
+    largest bf16 below 65520): the prefix's P V keeps V in bf16 and carries P as hi + lo
+    terms, so outputs must match the oracle, with nothing flagged."""
+    step = W.shared_prefix_step("spr", W.Shape(16, 4, d, 16, "bf16"), 512, _suffixes(20, 40),
+                                [300], seed=41)
+    blocks = step.shared_prefix[0]
+    run = StepRun(step)
+    v = run.vals["v_cache"]
+    v[int(blocks[2]), 1, 3, 5] = -1.0e5   # prefix tile 0 (tokens 32..47), KV head 1
+    v[int(blocks[20]), 3, 0, 0] = 3.0e6   # prefix tile 2 (token 320), KV head 3
+    v[int(blocks[9]), 0, 7, 2] = 65280.0  # prefix tile 1, KV head 0: fits fp16
+    kc, vc = run.host_pool()
+    vals = run.host_values()
+    res = run.run(share_prefix=True)
+    assert pa.get_status() == 0
+    ref = oracle_step(step, kc, vc, vals)
+    got = to_f64(res["out_decode"])
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref["out_decode"]).max() <= _wide_tol(3.0e6)
+
+
 def test_many_sequences_and_sharers(pa):
     """1,200 sequences (more than the plan kernel has threads), 1,000 of them on one
     prefix: sharer flags and reserved partial slots over many sequences per thread."""
