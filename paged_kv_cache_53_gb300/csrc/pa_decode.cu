@@ -140,23 +140,33 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
 
   // sequences reading a shared prefix start their own partitions after it and keep
-  // pre.splits partial slots, ahead of those, for the prefix's partials
+  // pre.splits partial slots, ahead of those, for the prefix's partials.  Which sequences
+  // they are is read in every pass below: from shared memory for batches of up to
+  // kSufCache sequences, from the workspace beyond.
+  __shared__ unsigned char s_flag[kSufCache];
+  const bool flags_shared = num_seqs <= kSufCache;
   if (pre.num_sharers > 0) {
-    for (int b = tid; b < num_seqs; b += blockDim.x) ws.seq_flags[b] = 0;
+    for (int b = tid; b < num_seqs; b += blockDim.x) {
+      if (flags_shared) s_flag[b] = 0;
+      else ws.seq_flags[b] = 0;
+    }
     __syncthreads();
     for (int i = tid; i < pre.num_sharers; i += blockDim.x) {
       const int sb = pre.sharers[i];
-      if (sb >= 0 && sb < num_seqs) ws.seq_flags[sb] = 1;
-      else flag_status(status, PA_STATUS_BAD_CONTEXT);
+      if (sb >= 0 && sb < num_seqs) {
+        if (flags_shared) s_flag[sb] = 1;
+        else ws.seq_flags[sb] = 1;
+      } else {
+        flag_status(status, PA_STATUS_BAD_CONTEXT);
+      }
     }
     __syncthreads();
   }
-  auto start_of = [&](int b) {
-    return (pre.num_sharers > 0 && ws.seq_flags[b]) ? pre.prefix_len : 0;
+  auto sharer = [&](int b) {
+    return pre.num_sharers > 0 && (flags_shared ? s_flag[b] != 0 : ws.seq_flags[b] != 0);
   };
-  auto reserved_of = [&](int b) {
-    return (pre.num_sharers > 0 && ws.seq_flags[b]) ? pre.splits : 0;
-  };
+  auto start_of = [&](int b) { return sharer(b) ? pre.prefix_len : 0; };
+  auto reserved_of = [&](int b) { return sharer(b) ? pre.splits : 0; };
 
   long long sum = 0;
   for (int b = b0; b < b1; ++b) {

@@ -120,13 +120,16 @@ def test_v_beyond_fp16_range_in_the_prefix(pa, d):
     assert np.abs(got - ref["out_decode"]).max() <= _wide_tol(3.0e6)
 
 
-def test_many_sequences_and_sharers(pa):
+@pytest.mark.parametrize("n_sharers,n_others", [(1000, 200), (4300, 200)])
+def test_many_sequences_and_sharers(pa, n_sharers, n_others):
     """1,200 sequences (more than the plan kernel has threads), 1,000 of them on one
-    prefix: sharer flags and reserved partial slots over many sequences per thread."""
-    rng = np.random.default_rng(38)
+    prefix: sharer flags and reserved partial slots over many sequences per thread; and
+    4,500 sequences, past the 4,096 whose sharer flags the plan keeps in shared memory
+    (beyond, it keeps them in the workspace)."""
+    rng = np.random.default_rng(38 + n_sharers)
     step = W.shared_prefix_step("spmany", W.Shape(32, 8, 64, 16, "bf16"), 512,
-                                rng.integers(1, 40, size=1000), rng.integers(1, 600, size=200),
-                                seed=38)
+                                rng.integers(1, 40, size=n_sharers),
+                                rng.integers(1, 600, size=n_others), seed=38)
     _check(pa, step)
 
 
