@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
   const int per = (num_seqs + blockDim.x - 1) / blockDim.x;
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+  // the thread's first context length, loaded while the sharer flags are set up (an input
+  // of the call: no kernel before this one writes it)
+  const int c_first = b0 < b1 ? __ldcg(context_lens + b0) : 0;
 
   // sequences reading a shared prefix start their own partitions after it and keep
   // pre.splits partial slots, ahead of those, for the prefix's partials.  Which sequences
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
 
   long long sum = 0;
   for (int b = b0; b < b1; ++b) {
-    const int c = __ldcg(context_lens + b);
+    const int c = b == b0 ? c_first : __ldcg(context_lens + b);
     if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
     const int cc = clamp_ctx(c, ctx_cap), st = start_of(b);
     if (cc < st) flag_status(status, PA_STATUS_BAD_CONTEXT);
