@@ -132,6 +132,16 @@ def test_prefill_rejects_bad_arguments(lib):
     assert lib.pa_prefill_chunk(*args) == 1
 
 
+def test_prefill_with_nothing_to_do_is_a_no_op(lib):
+    """No sequences, or no new tokens: nothing is launched (and no device is touched)."""
+    base = [None, 2, None, None, None, None, 8, None, None, 0, 16, 8, 128, 32, 8, 128, 16, 64,
+            0.1, 2, None, 0, None]
+    assert lib.pa_prefill_chunk(*base) == 0          # num_seqs = 0
+    no_tokens = list(base)
+    no_tokens[9], no_tokens[10] = 4, 0               # 4 sequences, 0 new tokens
+    assert lib.pa_prefill_chunk(*no_tokens) == 0
+
+
 def test_cache_ops_reject_bad_arguments(lib):
     assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 100, 16, 64, 2, None) == 2
     assert lib.pa_reshape_and_cache(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 8, 128, 16, 64, 2,

@@ -58,6 +58,15 @@ def test_prefill_shapes(pa, dtype, d, bs, h_q, h_kv):
     _check(pa, step)
 
 
+def test_prefill_zero_token_chunks(pa):
+    """Sequences that append nothing this step sit between ones that do: they get no
+    rows and change nothing; the others match the oracle."""
+    chunks = [0, 7, 0, 1, 130, 0]
+    ctx = [50, 67, 1, 1, 130, 300]
+    step = W.prefill_step("pz", W.Shape(32, 8, 128, 16, "bf16"), ctx, chunks, seed=39)
+    _check(pa, step)
+
+
 def test_prefill_many_sequences(pa):
     """More sequences than the plan kernel has threads: 1,500 chunks of 1 to 6 tokens over
     contexts of up to 200 tokens (one work item each per KV head)."""
