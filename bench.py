@@ -988,34 +988,6 @@ def _oracle_payload(step: W.Step, seqs, gen):
     return (q, kc, vc, tables, ctx, step.scale, sh.dtype)
 
 
-def make_oracle_sample(step: W.Step, budget_s: float, cores: int):
-    """Chooses a sample of sequences worth about `budget_s` seconds of oracle work per
-    core (measured on one sequence first) and splits it into per-worker payloads."""
-    import torch
-    d = step.decode
-    gen = torch.Generator().manual_seed(step.seed)
-    order = np.random.default_rng(7).permutation(d.num_seqs)
-    probe = _oracle_payload(step, [int(order[0])], gen)
-    secs, toks = _oracle_worker(probe)
-    per_token = secs / max(1, toks)
-    want = budget_s * cores / max(per_token, 1e-9)
-    seqs, tok = [], 0
-    for s in order:
-        if seqs and tok >= want:
-            break
-        seqs.append(int(s))
-        tok += int(d.context_lens[s])
-    reps = max(1, int(round(want / max(tok, 1))))  # the whole batch is cheaper: repeat it
-    chunks = [c for c in (seqs[i::cores] for i in range(cores)) if c]
-    payloads = [_oracle_payload(step, c, gen) for c in chunks] * reps
-    tok *= reps
-    kvb = tok * 2 * step.shape.num_kv_heads * step.shape.head_dim * step.shape.elem_bytes
-    desc = (f"{len(seqs)} of {d.num_seqs} sequences ({tok // reps} of "
-            f"{int(d.context_lens.sum())} KV tokens) of the same workload, run {reps}x; "
-            f"float64 numpy oracle in {len(chunks)} spawned single-threaded workers")
-    return payloads, desc, kvb
-
-
 class OraclePool:
     """A spawned pool of single-threaded workers (started with spawn, so it is safe
     after CUDA is initialised)."""
@@ -1034,11 +1006,6 @@ class OraclePool:
                     os.environ.pop(k, None)
                 else:
                     os.environ[k] = v
-
-    def time(self, payloads):
-        t = time.perf_counter()
-        self.pool.map(_oracle_worker, payloads, chunksize=1)
-        return time.perf_counter() - t
 
     def close(self):
         self.pool.close()
@@ -1120,15 +1087,108 @@ def all_core_oracle(cores, names=("opt13b_decode", "llama8b_gqa_decode")):
     return res
 
 
-def cpu_baseline(step: W.Step, budget_s: float):
-    cores = host_cores()
-    payloads, desc, kvb = make_oracle_sample(step, budget_s, cores)
-    workers = min(cores, len(payloads))
-    pool = OraclePool(workers)
+# ---- all-core oracle runs with the inputs resident in the workers ----
+_W = {}  # per-worker state of a SyncOraclePool worker (a spawned process)
+
+
+def _sync_pool_init(barrier, counter):
+    _W["barrier"] = barrier
+    with counter.get_lock():
+        _W["k"] = counter.value
+        counter.value += 1
+
+
+def _oracle_sync_task(args):
+    """Worker k of n: builds its share (every n-th of the listed sequences) of workload
+    `name`'s decode batch once, waits until all n workers are ready (so that each holds
+    exactly one task of the round and all compute at once), then runs the oracle over it
+    `reps` times.  Returns (start, end, kv tokens) of the oracle's work, wall-clock."""
+    import torch
+    name, n, reps, seqs = args
+    k = _W["k"]
+    key = (name, n, len(seqs), seqs[0] if seqs else -1, seqs[-1] if seqs else -1)
+    if _W.get("key") != key:
+        step = W.NAMED[name]()
+        gen = torch.Generator().manual_seed(step.seed + 1000 + k)
+        mine = list(seqs)[k::n]
+        _W["payload"] = _oracle_payload(step, mine, gen) if mine else None
+        _W["key"] = key
+    _W["barrier"].wait(timeout=600)
+    t0 = time.time()
+    toks = 0
+    for _ in range(reps):
+        if _W["payload"] is not None:
+            toks += _oracle_worker(_W["payload"])[1]
+    return t0, time.time(), toks
+
+
+class SyncOraclePool:
+    """n spawned single-threaded workers, each holding its share of the inputs between
+    rounds, started together by a barrier: a round's wall time is the oracle's own, with no
+    inter-process transfer of inputs inside it."""
+
+    def __init__(self, n):
+        ctx = mp.get_context("spawn")
+        self.n = n
+        keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                               "MKL_NUM_THREADS")}
+        for k in keep:
+            os.environ[k] = "1"
+        try:
+            self.pool = ctx.Pool(n, initializer=_sync_pool_init,
+                                 initargs=(ctx.Barrier(n), ctx.Value("i", 0)))
+        finally:
+            for k, v in keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, name, seqs, reps=1):
+        out = self.pool.map(_oracle_sync_task, [(name, self.n, reps, seqs)] * self.n,
+                            chunksize=1)
+        return max(o[1] for o in out) - min(o[0] for o in out), sum(o[2] for o in out)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_sequences(step: W.Step, budget_s: float, cores: int):
+    """The decode batch's sequences worth about `budget_s` seconds of oracle work per core
+    (the cost of one token measured on one sequence first; the whole batch if it is
+    cheaper), and how many times to run them."""
+    import torch
+    d = step.decode
+    gen = torch.Generator().manual_seed(step.seed)
+    order = np.random.default_rng(7).permutation(d.num_seqs)
+    secs, toks = _oracle_worker(_oracle_payload(step, [int(order[0])], gen))
+    want = budget_s * cores * max(1, toks) / max(secs, 1e-9)
+    seqs, tok = [], 0
+    for s in order:
+        if seqs and tok >= want:
+            break
+        seqs.append(int(s))
+        tok += int(d.context_lens[s])
+    reps = max(1, int(round(want / max(tok, 1))))
+    return sorted(seqs), tok, reps
+
+
+def cpu_baseline(name: str, step: W.Step, budget_s: float):
+    cores = min(host_cores(), step.decode.num_seqs)
+    seqs, tok, reps = oracle_sequences(step, budget_s, cores)
+    pool = SyncOraclePool(cores)
     try:
-        wall = pool.time(payloads)
+        pool.run(name, seqs, 1)  # builds every worker's inputs (untimed)
+        wall, toks = pool.run(name, seqs, reps)
     finally:
         pool.close()
+    sh = step.shape
+    kvb = toks * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
+    desc = (f"{len(seqs)} of {step.decode.num_seqs} sequences ({tok} of "
+            f"{int(step.decode.context_lens.sum())} KV tokens) of the same workload, {reps}x, "
+            f"held by {cores} spawned single-threaded float64 numpy oracle workers started "
+            "together (inputs built before the timed round)")
     single = single_thread_oracle()
     single["how"] = ("one full pass of each workload's whole decode batch by one spawned "
                      "single-threaded worker, wall seconds of the oracle's work (input "
@@ -1137,26 +1197,33 @@ def cpu_baseline(step: W.Step, budget_s: float):
     allc["how"] = ("one full pass of each workload's whole decode batch by all workers at "
                    "once (every worker builds its share of the inputs first), wall seconds "
                    "from the first worker's start to the last one's end")
-    return {"value": round(kvb / wall / 1e9, 4), "unit": "GB/s", "cores": workers,
+    return {"value": round(kvb / wall / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "sample": desc, "seconds": round(wall, 2),
             "single_thread": single, "all_core": allc}
 
 
 def run_reference(args, world):
     step = W.NAMED[args.workload]()
-    cores = host_cores()
+    cores = min(host_cores(), step.decode.num_seqs)
     per_step = min(2.0, max(0.02, args.ref_total_s / max(1, args.steps + args.warmup)))
-    payloads, desc, kvb = make_oracle_sample(step, per_step, cores)
-    workers = min(cores, len(payloads))
-    pool = OraclePool(workers)
+    seqs, tok, reps = oracle_sequences(step, per_step, cores)
+    pool = SyncOraclePool(cores)
     try:
+        pool.run(args.workload, seqs, 1)  # builds every worker's inputs (untimed)
         for _ in range(args.warmup):
-            pool.time(payloads)
-        walls = [pool.time(payloads) for _ in range(args.steps)]
+            pool.run(args.workload, seqs, reps)
+        runs = [pool.run(args.workload, seqs, reps) for _ in range(args.steps)]
     finally:
         pool.close()
-    wall = float(np.mean(walls))
+    wall = float(np.mean([r[0] for r in runs]))
+    sh = step.shape
+    kvb = runs[0][1] * 2 * sh.num_kv_heads * sh.head_dim * sh.elem_bytes
     gbs = kvb / wall / 1e9
+    workers = cores
+    desc = (f"{len(seqs)} of {step.decode.num_seqs} sequences ({tok} of "
+            f"{int(step.decode.context_lens.sum())} KV tokens) of the same workload, {reps}x "
+            f"per step, held by {cores} spawned single-threaded float64 numpy oracle workers "
+            "started together (inputs built before the timed steps)")
     full = kv_bytes(step)
     return {
         "impl": "reference",
@@ -1261,7 +1328,7 @@ def main():
         import torch
         res.update(run_extras(args, torch.device("cuda", local_rank)))
     if rank == 0 and not args.no_cpu_baseline and world == 1 and step.decode is not None:
-        res["cpu_baseline"] = cpu_baseline(step, args.cpu_budget_s)
+        res["cpu_baseline"] = cpu_baseline(args.workload, step, args.cpu_budget_s)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
