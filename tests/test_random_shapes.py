@@ -3,8 +3,9 @@
 Each case draws, from a fixed seed (every run checks the same cases), a dtype, head dim,
 block size, query / KV head counts and a ragged set of lengths that favours the edges (1,
 a block, a block +- 1, a 128-token tile +- 1), for decode, chunked prefill and
-shared-prefix decode.  The bars are those of the dedicated tests: max |gpu - oracle| <=
-2e-3 for fp16/bf16 inputs and 1e-5 for fp32 inputs, on fp32 outputs.
+shared-prefix decode.  The bars are those of the dedicated tests: the step's cache writes
+bit for bit, and max |gpu - oracle| <= 2e-3 for fp16/bf16 inputs and 1e-5 for fp32 inputs,
+on fp32 outputs.
 """
 import numpy as np
 import pytest
@@ -45,6 +46,9 @@ def _compare(pa, step, kind):
     vals = run.host_values()
     res = run.run(kinds=(kind,), share_prefix=step.shared_prefix is not None)
     ref = oracle_step(step, kc, vc, vals)
+    # the step's cache writes, bit for bit (the oracle applied them to its copy of the pool)
+    assert np.array_equal(W.to_numpy(run.vals["k_cache"]), kc)
+    assert np.array_equal(W.to_numpy(run.vals["v_cache"]), vc)
     got = to_f64(res[f"out_{kind}"])
     assert np.isfinite(got).all()
     err = max_abs_err(got, ref[f"out_{kind}"])
