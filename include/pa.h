@@ -289,11 +289,14 @@ int pa_decode_append(void* out, pa_dtype out_dtype, const void* q, const void* k
  * Sequences may point their tables at the same physical blocks when they share a prompt
  * prefix ("Continuous batching, paged attention, prefix caching", section "Prefix
  * caching": the server keeps one physical copy and points both block tables at it).
- * The result is exactly pa_decode's; the work differs: the prefix's attention is
- * computed once per KV head for all the sequences reading it, as one dense contraction
- * of all their query groups with the prefix's K/V on the tensor cores, and merged with
- * each sequence's own remaining context by log-sum-exp rescaling.  The prefix's K/V are
- * read from HBM once instead of once per sequence.
+ * The result is the same attention as pa_decode's, within the same error bound (the
+ * two differ in summation order and rounding, not in what they compute); the work
+ * differs: the prefix's attention is computed once per KV head for all the sequences
+ * reading it, as one dense contraction of all their query groups with the prefix's K/V on
+ * the tensor cores, and merged with each sequence's own remaining context by log-sum-exp
+ * rescaling.  The prefix's K/V are read from HBM once instead of once per sequence.  In
+ * the prefix's P V, P is one fp16 term for fp16 caches (unit roundoff 2^-11) and a pair
+ * of bf16 hi + lo terms for bf16 caches (relative error 2^-17), V as stored.
  *
  *   prefix_blocks  int32 [prefix_len / block_size], the prefix's physical blocks, device
  *   prefix_len     tokens of the prefix, a multiple of block_size
