@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   }
   griddep_launch_dependents();
   __shared__ long long s_sum[32];
+  __shared__ int s_smax[32];
   __shared__ int s_off[32], s_foff[32];
   __shared__ int s_ftotal;
   __shared__ int s_hist[kMaxPartBlocks + 2];
@@ -172,27 +173,49 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
   auto reserved_of = [&](int b) { return sharer(b) ? pre.splits : 0; };
 
   long long sum = 0;
+  int smax = 0;  // the longest own context of a sequence reading the shared prefix
   for (int b = b0; b < b1; ++b) {
     const int c = b == b0 ? c_first : __ldcg(context_lens + b);
     if (c < 0 || c > ctx_cap) flag_status(status, PA_STATUS_BAD_CONTEXT);
     const int cc = clamp_ctx(c, ctx_cap), st = start_of(b);
     if (cc < st) flag_status(status, PA_STATUS_BAD_CONTEXT);
     sum += max(0, cc - st);
+    if (st > 0) smax = max(smax, cc - st);
     if (b < kSufCache) s_suf[b] = max(0, cc - st);
     if (cc == 0 && reserved_of(b) == 0)  // an empty context attends to nothing: zeros
       for (int i = 0; i < out_row_vec16; ++i) out[(size_t)b * out_row_vec16 + i] = make_int4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
-  if (lane == 0) s_sum[wid] = sum;
+  for (int o = 16; o; o >>= 1) {
+    sum += __shfl_xor_sync(~0u, sum, o);
+    smax = max(smax, __shfl_xor_sync(~0u, smax, o));
+  }
+  if (lane == 0) {
+    s_sum[wid] = sum;
+    s_smax[wid] = smax;
+  }
   for (int i = tid; i < kMaxPartBlocks + 2; i += blockDim.x) s_hist[i] = 0;
   if (tid == 0) s_nmerge = 0;
   __syncthreads();
   if (wid == 0) {
     long long total = lane < nwarps ? s_sum[lane] : 0;
+    int tmax = lane < nwarps ? s_smax[lane] : 0;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(~0u, total, o);
-    if (lane == 0) s_psz = partition_tokens(total, num_kv_heads, block_size, forced_psz);
+    for (int o = 16; o; o >>= 1) {
+      total += __shfl_xor_sync(~0u, total, o);
+      tmax = max(tmax, __shfl_xor_sync(~0u, tmax, o));
+    }
+    if (lane == 0) {
+      int psz = partition_tokens(total, num_kv_heads, block_size, forced_psz);
+      // partitions long enough that every sharer's partials (its prefix splits and its
+      // own partitions) are merged in one round
+      if (forced_psz <= 0 && pre.num_sharers > 0 && pre.max_own_parts > 0 && tmax > psz) {
+        long long need = (tmax + pre.max_own_parts - 1) / pre.max_own_parts;
+        need = (need + block_size - 1) / block_size * block_size;
+        psz = (int)max((long long)psz, min(need, (long long)kMaxPartBlocks * block_size));
+      }
+      s_psz = psz;
+    }
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
@@ -388,6 +411,8 @@ constexpr int kMaxGroup = 16;
 // Sequences with up to this many partitions are merged with one round of loads (D = 64;
 // six for D = 128, within the merge kernel's 64 registers a thread).
 constexpr int kMergeOneRound = 8;
+// the partials merge_row takes in one round for head dim D
+constexpr int merge_one_round(int D) { return D == 128 ? 6 : kMergeOneRound; }
 // Merge grid: CTAs of 256 threads per SM (at most 64 registers a thread, so that four
 // fit in the register file).
 constexpr int kMergeCtasPerSm = 4;
@@ -415,7 +440,7 @@ template <int D, typename TO>
 __device__ __forceinline__ void merge_row(const DecodeParams& p, int b, int hq, int ps, int np,
                                           TO* out, int lane) {
   constexpr int C = D / 32;
-  constexpr int R = C == 4 ? 6 : kMergeOneRound;
+  constexpr int R = merge_one_round(D);
   const size_t hs = (size_t)p.num_q_heads;
   const float2* ml = p.ws.part_ml + (size_t)ps * hs + hq;  // stride hs per partition
   const float* src = p.ws.part_acc + ((size_t)ps * hs + hq) * D + lane * C;
@@ -1454,9 +1479,11 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
   // one CTA; a thread per sequence up to 1,024 threads (fewer warps meet in its barriers)
   const int plan_threads = std::min(1024, std::max(32, (a.num_seqs + 31) / 32 * 32));
+  PrefixPlan pre = a.prefix;
+  pre.max_own_parts = merge_one_round(a.head_dim) - pre.splits;
   cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(plan_threads), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
-                             static_cast<int4*>(a.out), out_row_vec16, a.prefix,
+                             static_cast<int4*>(a.out), out_row_vec16, pre,
                              a.plan_wait_late ? 1 : 0, a.forced_part_tokens);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
   if (a.prefix.num_sharers > 0) {

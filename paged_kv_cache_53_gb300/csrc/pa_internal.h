@@ -117,6 +117,9 @@ struct PrefixPlan {
   const int32_t* sharers;
   const int32_t* prefix_blocks;
   int num_sharers, prefix_len, splits, split_tokens;
+  // set at launch: own partitions a sharer may have so that, with its `splits` prefix
+  // partials, the merge takes every partial of it in one round (<= 0: no limit)
+  int max_own_parts;
 };
 
 // forced_psz > 0: every partition has that many tokens (the testing entry point)
