@@ -31,6 +31,7 @@
 // therefore aims at bytes in flight (up to 192 KiB of TMA copies per SM) and keeps the
 // per-tile instruction count small.
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "pa_device.cuh"
@@ -68,6 +69,12 @@ struct DecodeParams {
   // for the kernel launched just before it (the shared prefix's) only before it exits.
   int plan_flag;
   int forced_psz;  // partition size set by the caller (tokens), 0: chosen from the batch
+  // With a shared prefix and `early` set, the producers start on the plan's first units
+  // before the plan is done (see early_records): the sharer list and the prefix's
+  // geometry, as the plan has them.
+  const int32_t* sharers;
+  int num_sharers, prefix_len, prefix_splits, max_own_parts;
+  int early;
 };
 
 // A unit as the producer hands it to its consumer.
@@ -92,6 +99,22 @@ __device__ __forceinline__ int partition_tokens(long long total, int num_kv_head
   return (int)want;
 }
 
+// The same with a shared prefix: partitions long enough that every sharer's partials (its
+// `max_own_parts` own partitions at most, beside its prefix splits) are merged in one
+// round.  `tmax` is the longest own context (past the prefix) of a sharer.
+__device__ __forceinline__ int batch_partition_tokens(long long total, int tmax,
+                                                      int num_kv_heads, int block_size,
+                                                      int forced, int num_sharers,
+                                                      int max_own_parts) {
+  int psz = partition_tokens(total, num_kv_heads, block_size, forced);
+  if (forced <= 0 && num_sharers > 0 && max_own_parts > 0 && tmax > psz) {
+    long long need = (tmax + max_own_parts - 1) / max_own_parts;
+    need = (need + block_size - 1) / block_size * block_size;
+    psz = (int)max((long long)psz, min(need, (long long)kMaxPartBlocks * block_size));
+  }
+  return psz;
+}
+
 // ----------------------------------------------------------------------------------
 // 1. plan
 // ----------------------------------------------------------------------------------
@@ -114,15 +137,17 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
                                                            DecodeWorkspace ws, int32_t* status,
                                                            int4* out, int out_row_vec16,
                                                            PrefixPlan pre, int wait_late,
-                                                           int forced_psz) {
+                                                           int forced_psz, int early) {
   // wait_late: the previous kernel on the stream writes nothing this kernel reads or
   // writes; it is waited for only at the end, so that the work list is built meanwhile
   // and the next kernel still starts after both (lengths are read through L2)
   if (!wait_late) griddep_wait();
   // with a shared prefix the attention kernel waits for the flag this kernel sets at its
-  // end: cleared before the kernels after this one may launch
+  // end: cleared before the kernels after this one may launch, like the counter of the
+  // units it takes before that flag (`early`: the full partitions, which head the list)
   if (pre.num_sharers > 0 && threadIdx.x == 0) {
     ws.header[5] = 0;
+    if (early) ws.header[6] = 0;
     __threadfence();
   }
   griddep_launch_dependents();
@@ -205,17 +230,9 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
       total += __shfl_xor_sync(~0u, total, o);
       tmax = max(tmax, __shfl_xor_sync(~0u, tmax, o));
     }
-    if (lane == 0) {
-      int psz = partition_tokens(total, num_kv_heads, block_size, forced_psz);
-      // partitions long enough that every sharer's partials (its prefix splits and its
-      // own partitions) are merged in one round
-      if (forced_psz <= 0 && pre.num_sharers > 0 && pre.max_own_parts > 0 && tmax > psz) {
-        long long need = (tmax + pre.max_own_parts - 1) / pre.max_own_parts;
-        need = (need + block_size - 1) / block_size * block_size;
-        psz = (int)max((long long)psz, min(need, (long long)kMaxPartBlocks * block_size));
-      }
-      s_psz = psz;
-    }
+    if (lane == 0)
+      s_psz = batch_partition_tokens(total, tmax, num_kv_heads, block_size, forced_psz,
+                                     pre.num_sharers, pre.max_own_parts);
   }
   __syncthreads();
   const int psz = s_psz, bpp = psz / block_size;
@@ -362,7 +379,9 @@ __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const int32_t* __r
     run += np + rs;
   }
   if (tid == 0) {
-    ws.header[0] = 0;
+    // with `early`, the attention kernel has taken the full partitions by a counter of its
+    // own: this list's counter starts past them
+    ws.header[0] = early ? s_ftotal * num_kv_heads : 0;
     ws.header[1] = s_units * num_kv_heads;
     ws.header[2] = psz;
     ws.header[3] = s_total;
@@ -875,6 +894,168 @@ __device__ void prefetch_first_units(const DecodeParams& p, int* scratch) {
   __syncthreads();  // the scratch is the K/V ring from here on
 }
 
+// Batches (with a shared prefix) of up to this many sequences let the attention kernel
+// derive the plan's first units itself.
+constexpr int kEarlyMaxSeqs = 1024;
+
+// Shared memory the attention kernel's own records take: three ints per sequence and a
+// reduction scratch.
+__host__ __device__ constexpr size_t early_table_bytes(int num_seqs) {
+  return ((size_t)(3 * num_seqs + 64) * sizeof(int) + 15) / 16 * 16;
+}
+
+// The attention kernel's own records of the plan's first units, in a batch with a shared
+// prefix.  The plan lists every sequence's full partitions (all but its last) first, in
+// sequence order, and their lengths and partial slots are functions of the context
+// lengths and the sharer list alone; each CTA evaluates the same functions here, into
+// `tab` (early_table_bytes(num_seqs) of shared memory), so that its producers can take
+// those units while the plan is still being built.  Returns the number of such units and
+// sets `psz` to the partition length.  Every thread of the CTA calls it.
+template <int NT>
+__device__ int early_records(const DecodeParams& p, int* tab, int block_size, int& psz) {
+  constexpr int kPer = kEarlyMaxSeqs / NT;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = p.num_seqs;
+  int* s_c = tab;          // own context length (past the prefix for a sharer)
+  int* s_f = tab + n;      // index of the sequence's first full partition in the list
+  int* s_r = tab + 2 * n;  // its first partial slot; bit 31: it reads the shared prefix
+  long long* s_sum = reinterpret_cast<long long*>(tab + 3 * n + (n & 1));  // 8-byte aligned
+  int* s_max = reinterpret_cast<int*>(s_sum + NT / 32);
+  int* s_a = s_max + NT / 32;
+  int* s_b = s_a + NT / 32;
+  static_assert(2 * (NT / 32) + 3 * (NT / 32) + 1 <= 64, "the scratch fits the table's tail");
+  // the lengths are loaded while the sharer flags are set up
+  int len[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int b = tid + k * NT;
+    len[k] = b < n ? __ldcg(p.context_lens + b) : 0;
+  }
+  for (int b = tid; b < n; b += NT) s_r[b] = 0;
+  __syncthreads();
+  for (int i = tid; i < p.num_sharers; i += NT) {
+    const int sb = __ldg(p.sharers + i);
+    if (sb >= 0 && sb < n) s_r[sb] = 1;  // (the plan flags an index outside the batch)
+  }
+  __syncthreads();
+  long long sum = 0;
+  int mx = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int b = tid + k * NT;
+    if (b < n) {
+      const int st = s_r[b] != 0 ? p.prefix_len : 0;
+      const int c = max(0, clamp_ctx(len[k], p.ctx_cap) - st);
+      s_c[b] = c;
+      sum += c;
+      if (st > 0) mx = max(mx, c);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    sum += __shfl_xor_sync(~0u, sum, o);
+    mx = max(mx, __shfl_xor_sync(~0u, mx, o));
+  }
+  if (lane == 0) {
+    s_sum[wid] = sum;
+    s_max[wid] = mx;
+  }
+  __syncthreads();
+  long long total = 0;
+  int tmax = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    total += s_sum[w];
+    tmax = max(tmax, s_max[w]);
+  }
+  psz = batch_partition_tokens(total, tmax, p.num_kv_heads, block_size, p.forced_psz,
+                               p.num_sharers, p.max_own_parts);
+  // exclusive scans, in sequence order, of the partial slots (own partitions and reserved
+  // prefix slots) and of the full partitions; threads own consecutive sequences
+  const int per = (n + NT - 1) / NT, b0 = min(n, tid * per), b1 = min(n, b0 + per);
+  int slots = 0, fulls = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int np = (s_c[b] + psz - 1) / psz;
+    slots += np + (s_r[b] != 0 ? p.prefix_splits : 0);
+    fulls += np > 1 ? np - 1 : 0;
+  }
+  int ia = slots, ib = fulls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ta = __shfl_up_sync(~0u, ia, o), tb = __shfl_up_sync(~0u, ib, o);
+    if (lane >= o) {
+      ia += ta;
+      ib += tb;
+    }
+  }
+  if (lane == 31) {
+    s_a[wid] = ia;
+    s_b[wid] = ib;
+  }
+  __syncthreads();
+  int ra = ia - slots, rb = ib - fulls, ftotal = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    if (w < wid) {
+      ra += s_a[w];
+      rb += s_b[w];
+    }
+    ftotal += s_b[w];
+  }
+  for (int b = b0; b < b1; ++b) {
+    const int np = (s_c[b] + psz - 1) / psz;
+    const bool sh = s_r[b] != 0;
+    s_f[b] = rb;
+    s_r[b] = ra | (sh ? (int)0x80000000u : 0);
+    ra += np + (sh ? p.prefix_splits : 0);
+    rb += np > 1 ? np - 1 : 0;
+  }
+  __syncthreads();
+  return ftotal * p.num_kv_heads;
+}
+
+// Unit u (below early_records' count) from the CTA's own records: full partition u / H_kv
+// of the list for KV head u % H_kv.
+__device__ __forceinline__ UnitDesc early_unit(const DecodeParams& p, const int* tab, int psz,
+                                               int u) {
+  const int n = p.num_seqs, hkv = p.num_kv_heads;
+  const int q = u / hkv;
+  int lo = 0, hi = n;  // the last sequence whose first full partition is <= q
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tab[n + mid] <= q) lo = mid + 1;
+    else hi = mid;
+  }
+  const int b = lo - 1;
+  const int r = tab[2 * n + b];
+  const bool sh = r < 0;
+  const int run = r & 0x7fffffff, rs = sh ? p.prefix_splits : 0;
+  const int i = q - tab[n + b];
+  UnitDesc d;
+  d.b = b;
+  d.h = u - q * hkv;
+  d.tok0 = (sh ? p.prefix_len : 0) + i * psz;
+  d.ntok = psz;
+  d.nparts = (tab[b] + psz - 1) / psz + rs;
+  d.part_idx = run + rs + i;
+  d.part_start = run;
+  d.valid = 1;
+  return d;
+}
+
+// Waits (bounded) for the plan's flag; returns the plan's unit count, 0 if it never came.
+__device__ __forceinline__ int wait_plan_units(const DecodeParams& p) {
+  const uint64_t t0 = global_timer_ns();
+  int v;
+  while ((v = ld_acquire_gpu(p.ws.header + 5)) == 0 && global_timer_ns() - t0 < kWaitTimeoutNs)
+    __nanosleep(128);
+  if (v == 0) {
+    flag_status(p.status, PA_STATUS_TIMEOUT);
+    return 0;
+  }
+  return __ldcg(p.ws.header + 1);
+}
+
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -925,8 +1106,16 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
       if (on) griddep_wait();
     }
   } wait_at_exit{p.plan_flag};
+  // with a shared prefix and `early`, the producers take the full partitions from the
+  // CTA's own records and wait for the plan only when those run out
+  int psz_early = 0, early_units = 0;
+  const int* early_tab = reinterpret_cast<const int*>(descs + C::kPairs * 2);
+  if (p.early)
+    early_units = early_records<C::kThreads>(p, reinterpret_cast<int*>(descs + C::kPairs * 2), BS,
+                                             psz_early);
   __shared__ int s_plan_ready;
-  if (p.plan_flag) {
+  if (p.early) {
+  } else if (p.plan_flag) {
     if (threadIdx.x == 0) {
       const uint64_t t0 = global_timer_ns();
       int v;
@@ -941,16 +1130,32 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
     __syncthreads();
     griddep_wait();  // the plan kernel's work list is complete from here on
   }
-  // (a plan that never finished leaves no work: the kernel only waits and exits)
-  const int total_units = !p.plan_flag || s_plan_ready ? __ldcg(p.ws.header + 1) : 0;
+  // (a plan that never finished leaves no work: the kernel only waits and exits; with
+  // `early`, lane 0 of each producer maps the end of the plan's list to INT_MAX)
+  const int total_units =
+      p.early ? INT_MAX : (!p.plan_flag || s_plan_ready ? __ldcg(p.ws.header + 1) : 0);
 
   if (warp >= C::kPairs) {
     // ------------------------------ producer warp ------------------------------
     const uint32_t qbytes = (uint32_t)G * D * sizeof(T);
     const uint64_t policy = l2_policy_evict_first();
     uint32_t tile_it = 0, q_it = 0;
+    // lane 0's claims: with `early`, first the full partitions by the early counter, then,
+    // once the plan's flag is up, the rest of its list (whose counter starts past them)
+    bool from_plan = !p.early;
+    int plan_units = 0;
+    auto claim = [&]() -> int {
+      if (!from_plan) {
+        const int u = atomicAdd(p.ws.header + 6, 1);
+        if (u < early_units) return u;
+        from_plan = true;
+        plan_units = wait_plan_units(p);
+      }
+      const int u = atomicAdd(p.ws.header, 1);
+      return p.early && u >= plan_units ? INT_MAX : u;
+    };
     int next_u = 0;
-    if (lane == 0) next_u = atomicAdd(p.ws.header, 1);
+    if (lane == 0) next_u = claim();
     next_u = __shfl_sync(~0u, next_u, 0);
     bool ok = true;
     while (ok) {
@@ -965,14 +1170,20 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
         griddep_launch_dependents();
         break;
       }
-      const UnitDesc d = describe_unit(load_part(p, u), u, p.num_kv_heads);
+      UnitDesc d;
+      if (u < early_units) {
+        d = early_unit(p, early_tab, psz_early, u);
+      } else {
+        if (p.early) __syncwarp();  // lane 0 saw the plan's flag: its list is visible
+        d = describe_unit(load_part(p, u), u, p.num_kv_heads);
+      }
       const int ntiles = (d.ntok + BS - 1) / BS;
       // The next unit is claimed when about a ring's worth of this unit's tiles is left to
       // issue: early enough to load its record and block list while those are consumed,
       // late enough that near the end of the list no unit waits behind a busy pair while
       // others have run out.
       const int claim_at = ntiles > S ? ntiles - S : 0;
-      if (ntiles == 0 && lane == 0) next_u = atomicAdd(p.ws.header, 1);
+      if (ntiles == 0 && lane == 0) next_u = claim();
       const int32_t* row = p.block_tables + (size_t)d.b * p.max_blocks + d.tok0 / BS;
       int ids[kMaxPartBlocks / 32];
 #pragma unroll
@@ -998,7 +1209,7 @@ __global__ void __launch_bounds__(MmaCfg<D, BS, 2>::kThreads, 1)
       }
       ++q_it;
       for (int t = 0; t < ntiles; ++t) {
-        if (t == claim_at && lane == 0) next_u = atomicAdd(p.ws.header, 1);
+        if (t == claim_at && lane == 0) next_u = claim();
         const int s = tile_it % S;
         if (!mbar_wait(smem_addr(empty + s), ((tile_it / S) & 1) ^ 1)) { ok = false; break; }
         const int k = t >> 5;
@@ -1372,10 +1583,28 @@ int launch_mma(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) 
   const int occ = configure(slot, dev, C::kThreads, slot.smem_max);
   if (occ < 0) return fail(PA_ERR_CUDA, "pa_decode: kernel configuration failed");
   const int grid = a.max_ctas > 0 ? std::min(a.max_ctas, sm_count() * occ) : sm_count() * occ;
+  const size_t smem = C::smem_bytes(p.group) + (p.early ? early_table_bytes(p.num_seqs) : 0);
   const cudaError_t e = launch_pdl(decode_mma_kernel<T, D, BS>, dim3(grid), dim3(C::kThreads),
-                                   C::smem_bytes(p.group), stream, tmk, tmv, p);
+                                   smem, stream, tmk, tmv, p);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(e));
   return PA_OK;
+}
+
+// Whether the attention kernel's own records of the plan's first units fit beside its
+// rings (within the shared memory its launches are configured for).
+bool early_table_fits(int head_dim, int block_size, int group, int num_seqs) {
+  auto fits = [&](size_t base, size_t limit) {
+    return base + early_table_bytes(num_seqs) <= limit;
+  };
+  if (head_dim == 128 && block_size == 16)
+    return fits(MmaCfg<128, 16, 2>::smem_bytes(group), MmaCfg<128, 16, 2>::smem_bytes(kMaxGroup));
+  if (head_dim == 128 && block_size == 32)
+    return fits(MmaCfg<128, 32, 2>::smem_bytes(group), MmaCfg<128, 32, 2>::smem_bytes(kMaxGroup));
+  if (head_dim == 64 && block_size == 16)
+    return fits(MmaCfg<64, 16, 2>::smem_bytes(group), MmaCfg<64, 16, 2>::smem_bytes(kMaxGroup));
+  if (head_dim == 64 && block_size == 32)
+    return fits(MmaCfg<64, 32, 2>::smem_bytes(group), MmaCfg<64, 32, 2>::smem_bytes(kMaxGroup));
+  return false;
 }
 
 template <typename T>
@@ -1481,10 +1710,17 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int plan_threads = std::min(1024, std::max(32, (a.num_seqs + 31) / 32 * 32));
   PrefixPlan pre = a.prefix;
   pre.max_own_parts = merge_one_round(a.head_dim) - pre.splits;
+  // With a shared prefix the attention kernel may take the plan's first units from its
+  // own records (not when the plan waits for the kernel before it only at its end: the
+  // attention kernel would then start before that kernel is done)
+  const bool early = a.prefix.num_sharers > 0 && !a.plan_wait_late && a.dtype != PA_F32 &&
+                     a.num_seqs <= kEarlyMaxSeqs &&
+                     early_table_fits(a.head_dim, a.block_size, a.num_q_heads / a.num_kv_heads,
+                                      a.num_seqs);
   cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(plan_threads), 0, stream, a.context_lens,
                              a.num_seqs, ctx_cap, a.num_kv_heads, a.block_size, a.ws, a.status,
                              static_cast<int4*>(a.out), out_row_vec16, pre,
-                             a.plan_wait_late ? 1 : 0, a.forced_part_tokens);
+                             a.plan_wait_late ? 1 : 0, a.forced_part_tokens, early ? 1 : 0);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode (plan): %s", cudaGetErrorString(e));
   if (a.prefix.num_sharers > 0) {
     const int rc = launch_shared_prefix(a, stream);
@@ -1515,6 +1751,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.prefetch_bytes = a.prefix.num_sharers > 0 ? 0 : kDecodePrefetchBytes;
   p.plan_flag = a.prefix.num_sharers > 0;
   p.forced_psz = a.forced_part_tokens;
+  p.sharers = pre.sharers;
+  p.num_sharers = pre.num_sharers;
+  p.prefix_len = pre.prefix_len;
+  p.prefix_splits = pre.splits;
+  p.max_own_parts = pre.max_own_parts;
+  p.early = early ? 1 : 0;
 
   int rc = PA_OK;
   if (a.dtype == PA_F32) {

@@ -12,8 +12,8 @@
 //
 // CTA (pair, split, h) owns two 128-row query tiles; row r of the pair is sharer
 // (pair * 256 + r) / G, query head h * G + r % G.  The pipeline is the chunked-prefill
-// kernel's: a TMA producer warp streams 128-token K/V tiles of the prefix through the
-// prefix's block list into a ring; one warp issues S = Q K^T and O += P V with P written
+// kernel's: a TMA producer warp streams 128-token K and V tiles of the prefix through the
+// prefix's block list into a K ring and a V ring; one warp issues S = Q K^T and O += P V with P written
 // into S's TMEM columns; two softmax warpgroups, one per query tile, run the online
 // softmax.  The query rows are gathered from scattered sequences, so every thread of the
 // CTA copies a share of them into 128-byte-swizzled shared memory before the pipeline
@@ -45,18 +45,22 @@ struct SpCfg {
   static constexpr int kQHalfBytes = BM * 128;
   static constexpr int kQBytes = kHalves * kQHalfBytes;
   static constexpr int kKvHalfBytes = BN * 128;
-  static constexpr int kKBytes = kHalves * kKvHalfBytes;
-  static constexpr int kStageBytes = 2 * kKBytes;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kKBytes = kHalves * kKvHalfBytes;  // one K (or V) tile
+  // K and V tiles in rings of their own: K(j) is free once both S(j) products are done,
+  // a step before V(j), so its next tile loads a step earlier than in a shared ring
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr int kBlocksPerTile = BN / BS;
   static constexpr int kThreads = 384;
   static constexpr int kTmemCols = 512;
-  // kv_full[S], kv_empty[S], then per query tile s_full, p_full, pv_done, then q_full
-  static constexpr int kBars = 2 * kStages + 3 * kTiles + 1;
+  // k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per query tile s_full, p_full,
+  // pv_done, then q_full
+  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 3 * kTiles + 1;
   static constexpr int kGatherThreads = kThreads - 32;  // every warp but the producer
   static constexpr int kMaxSharers = kTiles * BM;  // sequences whose rows one CTA takes
-  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes + (size_t)kStages * kStageBytes +
-                                  kBars * 8 + 16 + kMaxSharers * 4;
+  static constexpr size_t kSmem = 1024 + kTiles * (size_t)kQBytes +
+                                  (size_t)(kKStages + kVStages) * kKBytes + kBars * 8 + 16 +
+                                  kMaxSharers * 4;
 };
 
 template <typename T>
@@ -88,18 +92,21 @@ __global__ void __launch_bounds__(384, 1)
     shared_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const SpParams p) {
   using C = SpCfg<D, BS>;
-  constexpr int BN = C::BN, S = C::kStages, NT = C::kTiles;
+  constexpr int BN = C::BN, SK = C::kKStages, SV = C::kVStages, NT = C::kTiles;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = base;
-  uint8_t* sKV = sQ + NT * C::kQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
+  uint8_t* sK = sQ + NT * C::kQBytes;
+  uint8_t* sV = sK + SK * C::kKBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kKBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
   int* s_seq = reinterpret_cast<int*>(tmem_slot + 4);  // [kMaxSharers]
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + S;
-  uint64_t* s_full = bars + 2 * S;
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + SK;
+  uint64_t* v_full = bars + 2 * SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* s_full = v_empty + SV;
   uint64_t* p_full = s_full + NT;
   uint64_t* pv_done = p_full + NT;
   uint64_t* q_full = pv_done + NT;
@@ -123,9 +130,13 @@ __global__ void __launch_bounds__(384, 1)
     s_seq[i] = sb >= 0 && sb < p.num_seqs ? sb : -1;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(kv_full + i), 1);
-      mbar_init(smem_addr(kv_empty + i), 1);
+    for (int i = 0; i < SK; ++i) {
+      mbar_init(smem_addr(k_full + i), 1);
+      mbar_init(smem_addr(k_empty + i), 1);
+    }
+    for (int i = 0; i < SV; ++i) {
+      mbar_init(smem_addr(v_full + i), 1);
+      mbar_init(smem_addr(v_empty + i), 1);
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(smem_addr(s_full + x), 1);
@@ -199,35 +210,53 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
+    // K(0), then V(j) and K(j + 1) for each j: the order in which the MMA warp frees
+    // their stages.  Lane i < kBlocksPerTile holds the id of a tile's i-th block; the ids
+    // of the tile after next are loaded while the current tiles are issued.
     const uint64_t keep = l2_policy_evict_last();  // the prefix is re-read by other CTAs
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j % S;
-      if (!mbar_wait(smem_addr(kv_empty + s), ((j / S) & 1) ^ 1)) { ok = false; break; }
+    auto tile_ids = [&](int j) {
       const int bi = (kv_begin + j * BN) / BS + lane;
       int id = -1;
-      if (lane < C::kBlocksPerTile && bi < nblk && bi * BS < kv_end) {
+      if (j < n_kv && lane < C::kBlocksPerTile && bi < nblk && bi * BS < kv_end) {
         id = __ldg(p.prefix_blocks + bi);
         if (id < 0 || id >= p.num_blocks) {
           flag_status(p.status, PA_STATUS_BAD_BLOCK);
           id = -1;
         }
       }
-      uint8_t* st = sKV + s * C::kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(smem_addr(kv_full + s), C::kStageBytes);
+      return id;
+    };
+    auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* full, int id) {
+      if (lane == 0) mbar_arrive_expect_tx(smem_addr(full), C::kKBytes);
 #pragma unroll
       for (int i = 0; i < C::kBlocksPerTile; ++i) {
         const int idi = __shfl_sync(~0u, id, i);
         if (lane == 0) {
+          // a bad block id reads a box that lies wholly outside the tensor: zeros
           const int y = idi < 0 ? -BS : (idi * p.num_kv_heads + h) * BS;
 #pragma unroll
-          for (int hb = 0; hb < C::kHalves; ++hb) {
-            const int off = hb * C::kKvHalfBytes + i * BS * 128;
-            tma_load_2d(smem_addr(st + off), &tmk, hb * 64, y, smem_addr(kv_full + s), keep);
-            tma_load_2d(smem_addr(st + C::kKBytes + off), &tmv, hb * 64, y,
-                        smem_addr(kv_full + s), keep);
-          }
+          for (int hb = 0; hb < C::kHalves; ++hb)
+            tma_load_2d(smem_addr(dst + hb * C::kKvHalfBytes + i * BS * 128), tm, hb * 64, y,
+                        smem_addr(full), keep);
         }
       }
+    };
+    int id_cur = tile_ids(0), id_next = tile_ids(1);
+    if (n_kv > 0) {
+      if (!mbar_wait(smem_addr(k_empty), 1)) ok = false;
+      else load_tile(&tmk, sK, k_full, id_cur);
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int sv = j % SV;
+      if (!mbar_wait(smem_addr(v_empty + sv), ((j / SV) & 1) ^ 1)) { ok = false; break; }
+      load_tile(&tmv, sV + sv * C::kKBytes, v_full + sv, id_cur);
+      if (j + 1 < n_kv) {
+        const int sk = (j + 1) % SK;
+        if (!mbar_wait(smem_addr(k_empty + sk), (((j + 1) / SK) & 1) ^ 1)) { ok = false; break; }
+        load_tile(&tmk, sK + sk * C::kKBytes, k_full + sk, id_next);
+      }
+      id_cur = id_next;
+      id_next = tile_ids(j + 2);
     }
     if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
   } else if (warp == 1) {
@@ -245,12 +274,12 @@ __global__ void __launch_bounds__(384, 1)
       // descriptors of each operand's first k-step and first stage, advanced by constant
       // offsets
       const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(sQ), 16, 1024);
-      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(sKV), 16, 1024);
-      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sKV + C::kKBytes), C::kKvHalfBytes, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(sK), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sV), C::kKvHalfBytes, 1024);
       auto issue_s = [&](int x, int s) {
         const uint32_t tS = tmem + x * BN;
         const uint64_t dq = tc::desc_advance(dq0, x * C::kQBytes);
-        const uint64_t dk = tc::desc_advance(dk0, s * C::kStageBytes);
+        const uint64_t dk = tc::desc_advance(dk0, s * C::kKBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
@@ -265,7 +294,7 @@ __global__ void __launch_bounds__(384, 1)
         tc::fence_after_sync();
         const uint32_t tP = tmem + x * BN;
         const uint32_t tO = tmem + NT * BN + x * D;
-        const uint64_t dv = tc::desc_advance(dv0, s * C::kStageBytes);
+        const uint64_t dv = tc::desc_advance(dv0, s * C::kKBytes);
         if constexpr (SpFmt<T>::v == 0) {
           // P: tokens 2c and 2c + 1 in column c
 #pragma unroll
@@ -285,34 +314,43 @@ __global__ void __launch_bounds__(384, 1)
         tc::commit_warp<false>(smem_addr(pv_done + x));
         return true;
       };
-      if (!wait_w(q_full, 0) || !wait_w(kv_full, 0)) ok = false;
-      if (ok) {
+      if (n_kv > 0 && (!wait_w(q_full, 0) || !wait_w(k_full, 0))) ok = false;
+      if (ok && n_kv > 0) {
         tc::fence_after_sync();
 #pragma unroll
         for (int x = 0; x < NT; ++x)
           if (valid[x]) issue_s(x, 0);
+        tc::commit_warp<false>(smem_addr(k_empty));  // K(0) is read by these alone
       }
-      // stage of step j and of step j + 1 (with its phase parity), without divisions
-      int s = 0, s1 = S > 1 ? 1 : 0;
-      uint32_t par1 = S > 1 ? 0 : 1;
+      // V stage of step j and K stage of step j + 1, with their phase parities, without
+      // divisions
+      int sv = 0, sk1 = SK > 1 ? 1 : 0;
+      uint32_t vpar = 0, kpar1 = SK > 1 ? 0 : 1;
       for (int j = 0; j < n_kv && ok; ++j) {
-        bool next_ready = false;
+        bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int x = 0; x < NT; ++x) {
           if (!valid[x]) continue;
-          if (!issue_pv(x, j, s)) { ok = false; break; }
+          if (!v_ready) {
+            if (!wait_w(v_full + sv, vpar)) { ok = false; break; }
+            tc::fence_after_sync();
+            v_ready = true;
+          }
+          if (!issue_pv(x, j, sv)) { ok = false; break; }
           if (j + 1 < n_kv) {
-            if (!next_ready) {
-              if (!wait_w(kv_full + s1, par1)) { ok = false; break; }
+            if (!k_ready) {
+              if (!wait_w(k_full + sk1, kpar1)) { ok = false; break; }
               tc::fence_after_sync();
-              next_ready = true;
+              k_ready = true;
             }
-            issue_s(x, s1);
+            issue_s(x, sk1);
           }
         }
-        tc::commit_warp<false>(smem_addr(kv_empty + s));
-        if (++s == S) s = 0;
-        if (++s1 == S) { s1 = 0; par1 ^= 1; }
+        if (!ok) break;
+        tc::commit_warp<false>(smem_addr(v_empty + sv));                 // V(j)
+        if (j + 1 < n_kv) tc::commit_warp<false>(smem_addr(k_empty + sk1));  // K(j + 1)
+        if (++sv == SV) { sv = 0; vpar ^= 1; }
+        if (++sk1 == SK) { sk1 = 0; kpar1 ^= 1; }
       }
       if (!ok && lane == 0) flag_status(p.status, PA_STATUS_TIMEOUT);
     }
