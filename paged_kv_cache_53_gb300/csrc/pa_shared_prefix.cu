@@ -370,93 +370,93 @@ __global__ void __launch_bounds__(384, 1)
       tc::fence_after_sync();
       const int kp0 = kv_begin + j * BN;
       const bool full = kp0 + BN <= kv_end;
-      // row maximum over the visible positions, the whole row's scores loaded behind one
-      // wait; on whole tiles with a positive scale the raw scores are compared and the
-      // maximum scaled once
+      // The row is processed in 32-column chunks by loops that are not unrolled: one
+      // chunk's code instead of four keeps the step's instructions within the instruction
+      // cache (unrolled, each step refetched most of them).
+      // Row maximum over the visible positions; on whole tiles with a positive scale the
+      // raw scores are compared and the maximum scaled once.
+      static_assert(BN == 128, "a 128-column row");
       float mx = kNegInf;
-      {
-        static_assert(BN == 128, "a 128-column row");
-        float c[4][32];
+      if (full && sc > 0.f) {
+#pragma unroll 1
+        for (int k = 0; k < BN / 32; ++k) {
+          float a[32];
+          tc::tmem_ld32(tS + 32 * k, a);
+          tc::tmem_wait_ld();
+          float r0 = a[0], r1 = a[1];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tc::tmem_ld32(tS + 32 * k, c[k]);
-        tc::tmem_wait_ld();
-        if (full && sc > 0.f) {
-          float rm[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            rm[k] = c[k][0];
-#pragma unroll
-            for (int i = 1; i < 32; ++i) rm[k] = fmaxf(rm[k], c[k][i]);
+          for (int i = 2; i < 32; i += 2) {
+            r0 = fmaxf(r0, a[i]);
+            r1 = fmaxf(r1, a[i + 1]);
           }
-          mx = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3])) * sc;
-        } else {
+          mx = fmaxf(mx, fmaxf(r0, r1));
+        }
+        mx *= sc;
+      } else {
+#pragma unroll 1
+        for (int k = 0; k < BN / 32; ++k) {
+          float a[32];
+          tc::tmem_ld32(tS + 32 * k, a);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              mx = fmaxf(mx, kp0 + 32 * k + i < kv_end ? c[k][i] * sc : kNegInf);
+          for (int i = 0; i < 32; ++i)
+            mx = fmaxf(mx, kp0 + 32 * k + i < kv_end ? a[i] * sc : kNegInf);
         }
       }
       const bool need = mx > m + kRescaleThreshold;
       const float alpha = need ? fast_exp2(m - mx) : 1.f;
       if (need) m = mx;
       // P = 2^(scale * S - m) over S's own columns: for fp16, one term, tokens 32k .. 32k+31
-      // in columns 16k .. 16k+15 (their scores are already in registers); for bf16, hi + lo
-      // terms in columns 32k .. 32k+31.  The next 32 columns load while these are
-      // exponentiated.
+      // in columns 16k .. 16k+15 (already read); for bf16, hi + lo terms in columns
+      // 32k .. 32k+31.
       constexpr bool wide = SpFmt<T>::v == 1;
       float sum = 0.f;
-      {
-        float buf[2][32];
-        tc::tmem_ld32(tS, buf[0]);
+#pragma unroll 1
+      for (int k = 0; k < BN / 32; ++k) {
+        float a[32];
+        tc::tmem_ld32(tS + 32 * k, a);
         tc::tmem_wait_ld();
+        const int c0 = 32 * k;
+        if (full) {
+          const uint64_t sc2 = f2(sc, sc), negm2 = f2(-m, -m);
 #pragma unroll
-        for (int k = 0; k < BN / 32; ++k) {
-          float (&a)[32] = buf[k & 1];
-          if (k + 1 < BN / 32) tc::tmem_ld32(tS + 32 * (k + 1), buf[(k + 1) & 1]);
-          const int c0 = 32 * k;
-          if (full) {
-            const uint64_t sc2 = f2(sc, sc), negm2 = f2(-m, -m);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float t0, t1;
-              f2_split(f2_fma(f2(a[2 * i], a[2 * i + 1]), sc2, negm2), t0, t1);
-              a[2 * i] = fast_exp2(t0);
-              a[2 * i + 1] = fast_exp2(t1);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            float t0, t1;
+            f2_split(f2_fma(f2(a[2 * i], a[2 * i + 1]), sc2, negm2), t0, t1);
+            a[2 * i] = fast_exp2(t0);
+            a[2 * i + 1] = fast_exp2(t1);
           }
-          float s2[2] = {0.f, 0.f};
-          if constexpr (!wide) {
-            uint32_t pk[16];
+        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              s2[i & 1] += a[2 * i] + a[2 * i + 1];
-              pk[i] = Mma<__half>::pack(a[2 * i], a[2 * i + 1]);
-            }
-            tc::tmem_st16(tS + 16 * k, pk);
-          } else {
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              s2[i & 1] += a[2 * i] + a[2 * i + 1];
-              hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
-            }
-            tc::tmem_st16(tS + c0, hi);
-            tc::tmem_st16(tS + c0 + 16, lo);
-          }
-          sum += s2[0] + s2[1];
-          if (k + 1 < BN / 32) tc::tmem_wait_ld();
+          for (int i = 0; i < 32; ++i)
+            a[i] = kp0 + c0 + i < kv_end ? fast_exp2(fmaf(a[i], sc, -m)) : 0.f;
         }
+        float s2[2] = {0.f, 0.f};
+        if constexpr (!wide) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            s2[i & 1] += a[2 * i] + a[2 * i + 1];
+            pk[i] = Mma<__half>::pack(a[2 * i], a[2 * i + 1]);
+          }
+          tc::tmem_st16(tS + 16 * k, pk);
+        } else {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            s2[i & 1] += a[2 * i] + a[2 * i + 1];
+            hi[i] = Mma<T>::pack_split(a[2 * i], a[2 * i + 1], lo[i]);
+          }
+          tc::tmem_st16(tS + c0, hi);
+          tc::tmem_st16(tS + c0 + 16, lo);
+        }
+        sum += s2[0] + s2[1];
       }
       l = l * alpha + sum;
       if (j >= 1 && __any_sync(~0u, need)) {
         if (!mbar_wait(smem_addr(pv_done + x), (j - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
           tc::tmem_ld32(tO + c0, o);
