@@ -1685,10 +1685,10 @@ PrefixPlan plan_prefix(int num_sharers, int prefix_len, int group, int num_kv_he
     pp.splits = 0;
     return pp;
   }
-  // about a third of the SMs (here 48 of 152): the attention over the sequences' own
-  // contexts takes the others meanwhile (a constant, so that the workspace size does
-  // not depend on the device)
-  constexpr int kTile = 128, kRowsPerCta = 256, kTargetCtas = 48;
+  // about 64 CTAs (42% of 152 SMs): the attention over the sequences' own contexts takes
+  // the other SMs meanwhile (a constant, so that the workspace size does not depend on
+  // the device)
+  constexpr int kTile = 128, kRowsPerCta = 256, kTargetCtas = 64;
   const long long row_ctas = ((long long)num_sharers * group + kRowsPerCta - 1) / kRowsPerCta;
   const long long tiles = (prefix_len + kTile - 1) / kTile;
   long long want = (kTargetCtas + row_ctas * num_kv_heads - 1) / (row_ctas * num_kv_heads);
