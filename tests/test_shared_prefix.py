@@ -66,7 +66,7 @@ def _suffixes(n, seed, hi=300, with_zero=True):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d,bs", [(128, 16), (128, 32), (64, 16), (64, 32)])
-@pytest.mark.parametrize("h_q,h_kv", [(32, 8), (8, 8), (16, 2)])
+@pytest.mark.parametrize("h_q,h_kv", [(32, 8), (8, 8), (16, 2), (32, 2)])
 def test_shapes(pa, dtype, d, bs, h_q, h_kv):
     # 592 = 37 blocks of 16 (not a whole number of 128-token tiles); 576 for block 32
     prefix = 592 if bs == 16 else 576
@@ -131,6 +131,57 @@ def test_many_sequences_and_sharers(pa, n_sharers, n_others):
                                 rng.integers(1, 40, size=n_sharers),
                                 rng.integers(1, 600, size=n_others), seed=38)
     _check(pa, step)
+
+
+@pytest.mark.parametrize("n_seqs", [1024, 1025])
+def test_early_records_boundary(pa, n_seqs):
+    """Batches of up to 1,024 sequences let the attention kernel take every sequence's full
+    partitions from its own records before the plan is done; one more and it waits for the
+    plan's list.  Both sides of the boundary, with many multi-partition sequences."""
+    rng = np.random.default_rng(41 + n_seqs)
+    n_sharers = 900
+    step = W.shared_prefix_step("spedge", W.Shape(32, 8, 64, 16, "bf16"), 256,
+                                rng.integers(1, 120, size=n_sharers),
+                                rng.integers(1, 300, size=n_seqs - n_sharers), seed=41)
+    _check(pa, step)
+
+
+def _shared_call(pa, run, ws):
+    """The shared-prefix decode of `run`'s step (its cache writes already done) into a
+    new fp32 output, on the workspace `ws`."""
+    st, sh = run.step, run.step.shape
+    b, m = st.decode, run.meta["decode"]
+    out = torch.empty((b.num_seqs, sh.num_q_heads, sh.head_dim), dtype=torch.float32,
+                      device=run.device)
+    blocks, plen, sharers = st.shared_prefix
+    pa.decode_shared_prefix(out, run.vals["q_decode"], run.vals["k_cache"], run.vals["v_cache"],
+                            m["bt"], m["ctx"], b.max_ctx, torch.from_numpy(blocks).to(run.device),
+                            plen, torch.from_numpy(sharers).to(run.device), st.scale, ws)
+    return out
+
+
+def test_workspace_reused_across_batches(pa):
+    """Two batches in turn on one workspace: one whose sequences have many full partitions
+    (taken before the plan is done, by a counter the plan resets every call) and one with
+    none.  Every call equals, bit for bit, the same call on a fresh workspace."""
+    shape = W.Shape(32, 8, 128, 16, "bf16")
+    rng = np.random.default_rng(43)
+    sa = W.shared_prefix_step("spa", shape, 1024, rng.integers(300, 900, size=96),
+                              rng.integers(500, 1500, size=16), seed=43)
+    sb = W.shared_prefix_step("spb", shape, 1024, rng.integers(1, 16, size=40), [5, 9],
+                              seed=44)
+    runs = [StepRun(sa), StepRun(sb)]
+    refs = [r.run(kinds=("decode",), share_prefix=True)["out_decode"] for r in runs]
+    nbytes = 0
+    for r in runs:
+        st, sh = r.step, r.step.shape
+        nbytes = max(nbytes, pa.decode_shared_prefix_workspace_bytes(
+            st.decode.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, st.decode.max_ctx,
+            sh.block_size, len(st.shared_prefix[2]), st.shared_prefix[1]))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=runs[0].device)
+    for i in (0, 1, 0, 1, 1, 0):
+        assert torch.equal(_shared_call(pa, runs[i], ws), refs[i]), i
+    assert pa.get_status() == 0
 
 
 def test_only_sharers_ending_at_the_prefix(pa):
