@@ -47,6 +47,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 GRAPH_STEP_MS = 0.1
 # bytes written between steps of the L2-flushed passes (L2: 129 MB)
 FLUSH_BYTES = 512 << 20
+# GPU cycles of the sleep queued ahead of each back-to-back pass (~100 us): the host
+# enqueues the pass's first calls meanwhile, so that the pass does not start with the GPU
+# waiting for them.
+PASS_LEAD_CYCLES = 200_000
 
 
 # ------------------------------------------------------------------ accounting
@@ -395,7 +399,11 @@ def run_ours(args, rank, world, local_rank):
             n += 1
         return n
 
+    # each pass is queued behind a short sleep kernel, outside its events, so that the host
+    # has queued the first steps when the pass starts (with few steps per pass, the GPU
+    # would otherwise wait one step's host latency inside the timed region)
     def plain_pass():
+        torch.cuda._sleep(PASS_LEAD_CYCLES)
         t0.record(stream)
         for i in range(k):
             one_step()
@@ -404,6 +412,7 @@ def run_ours(args, rank, world, local_rank):
         pass_ms.append(t0.elapsed_time(t1))
 
     def evented_pass():
+        torch.cuda._sleep(PASS_LEAD_CYCLES)
         t2.record(stream)
         for i in range(k):
             one_step(evs[i])
@@ -691,8 +700,11 @@ def _time_call(call, seconds: float, stream, dev, per_pass: int = 20, warmup: in
     `seconds` have passed, clocks sampled meanwhile: back-to-back passes with one event pair
     around the whole pass (as a serving loop issues its calls: each call's first kernels
     start while the previous call's last ones drain) give the median pass time per call;
-    evented passes, an event pair around each call (which ends that overlap), give the mean
-    per-call time.  Returns (back-to-back ms, evented ms, calls timed, clocks)."""
+    each such pass is queued behind a short sleep kernel, outside its events, so that the
+    host has queued its first calls when it starts (else a pass of short calls starts
+    with the GPU idle for the host's latency of one call); evented passes, an event pair
+    around each call (which ends that overlap), give the mean per-call time.  Returns
+    (back-to-back ms, evented ms, calls timed, clocks)."""
     import torch
     mk = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(warmup):
@@ -704,6 +716,7 @@ def _time_call(call, seconds: float, stream, dev, per_pass: int = 20, warmup: in
     with ClockSampler(dev.index or 0) as clocks:
         t_start = time.perf_counter()
         while not times or time.perf_counter() - t_start < seconds:
+            torch.cuda._sleep(PASS_LEAD_CYCLES)
             t0.record(stream)
             for _ in range(per_pass):
                 call()
